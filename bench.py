@@ -1,0 +1,413 @@
+"""Benchmark of the fused decode MoE layer: us per layer launch and achieved
+HBM GB/s against the byte roofline, one JSON line on stdout.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload dsv3_t1|dsv3_t8|dsv3_t64] [--sweep]
+
+A step is one launch of the whole layer (group table, gate/up + SwiGLU,
+down, router weights, shared expert, residual, bf16 write) over one batch.
+The default workload is the DeepSeek-V3-shaped decode layer at T=1 (H=7168,
+routed I=2048 NVFP4 E=256 top-8, shared I=2048 FP8 128x128 blocks, uniform
+routing). Four copies of the layer's weights are resident and the steps
+rotate over them, so each step reads weights that are not in L2 (126 MB).
+--impl reference times the fp64 CPU oracle on a bounded sample of the same
+workload (the reference arm). Under torchrun every rank runs its own replica
+(the build has no cross-GPU exchange); rank 0 prints the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOADS = {
+    "dsv3_t1": dict(T=1, routing="uniform"),
+    "dsv3_t8": dict(T=8, routing="mtp"),
+    "dsv3_t64": dict(T=64, routing="zipf"),
+}
+N_COPIES = 4
+KERNEL_SOURCES = ["moe_layer_decode_persistent_b300/csrc/api.cu",
+                  "moe_layer_decode_persistent_b300/csrc/fused_fma.cuh",
+                  "moe_layer_decode_persistent_b300/csrc/group_table.cuh",
+                  "moe_layer_decode_persistent_b300/csrc/moe_common.cuh"]
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        fp = os.path.join(ROOT, p)
+        if os.path.exists(fp):
+            h.update(open(fp, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6400.0, "fallback"
+
+
+def traffic_record(kernel: str):
+    """dram bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    rec = d.get(kernel)
+    if not rec or rec.get("source_hash") != kernel_source_hash():
+        return None
+    return rec
+
+
+class ClockSampler:
+    """nvidia-smi SM clock / throttle sampling during the timed region."""
+    Q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [v.strip() for v in ln.split(",")]
+            if len(f) < 6:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = max(mx, float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[2:6]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int, device=None) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def algorithmic_bytes(layer, ids) -> tuple[int, int]:
+    T, H, K = layer.shape.T, layer.shape.H, layer.shape.K
+    distinct = len(set(int(e) for e in ids.reshape(-1).tolist() if 0 <= int(e) < layer.shape.E))
+    b = distinct * layer.routed.nbytes_expert() + layer.shared.nbytes_expert() + 2 * T * H * 2 + T * K * 8
+    return b, distinct
+
+
+def run_ours(args, rank, world, local):
+    import torch
+
+    from moe_layer_decode_persistent_b300 import binding as B
+    from moe_layer_decode_persistent_b300 import build, inputs
+
+    build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = WORKLOADS[args.workload]
+    shape = inputs.dsv3(wl["T"])
+    L = inputs.make_layer(shape, wl["routing"], 0, dev, inputs.FMT_NVFP4, inputs.FMT_FP8_B128)
+    copies = [(L.routed, L.shared)]
+    for _ in range(N_COPIES - 1):
+        r = inputs.ExpertSet(**{k: (v.clone() if isinstance(v, torch.Tensor) else v)
+                                for k, v in L.routed.__dict__.items()})
+        s = inputs.ExpertSet(**{k: (v.clone() if isinstance(v, torch.Tensor) else v)
+                                for k, v in L.shared.__dict__.items()})
+        copies.append((r, s))
+    weights = [(B.make_weights(r), B.make_weights(s)) for r, s in copies]
+    sh = B.make_shape(shape.T, shape.H, shape.I, shape.I_shared, shape.E, shape.K, args.flags)
+    ws = torch.empty(B.moe_workspace_bytes_host(sh), dtype=torch.uint8, device=dev)
+    B.moe_workspace_init(ws)
+    out = torch.empty(shape.T, shape.H, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    algo_bytes, distinct = algorithmic_bytes(L, L.topk_ids.cpu())
+
+    def launch(i):
+        rw, sw = weights[i % N_COPIES]
+        B.moe_fused_decode(L.x, L.topk_ids, L.topk_w, rw, sw, out, sh, ws, stream=stream)
+
+    for i in range(args.warmup):
+        launch(i)
+    torch.cuda.synchronize()
+    assert B.moe_read_error(ws) == 0
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(args.steps):
+            starts[i].record(stream)
+            launch(i)
+            ends[i].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    err = B.moe_read_error(ws)
+    per_launch = [s.elapsed_time(e) * 1e3 for s, e in zip(starts, ends)]  # us
+    total_ms = t0.elapsed_time(t1)
+    ms_per_step = max_over_ranks(total_ms / args.steps, world, dev)
+    us_launch = statistics.mean(per_launch)
+    us_launch_max = max_over_ranks(us_launch, world, dev)
+
+    # end to end through the host-buffer entry point (pinned buffers, copies inside)
+    xh = L.x.cpu().pin_memory()
+    ih = L.topk_ids.cpu().pin_memory()
+    wh = L.topk_w.cpu().pin_memory()
+    oh = torch.empty_like(xh).pin_memory()
+
+    def launch_host(i):
+        rw, sw = weights[i % N_COPIES]
+        B.moe_fused_decode_host(xh, ih, wh, rw, sw, oh, sh, ws, stream=stream)
+
+    for i in range(max(3, args.warmup)):
+        launch_host(i)
+    barrier(world)
+    h0 = time.perf_counter()
+    for i in range(args.steps):
+        launch_host(i)
+    e2e_us = (time.perf_counter() - h0) / args.steps * 1e6
+    e2e_us = max_over_ranks(e2e_us, world, dev)
+    assert torch.equal(oh.view(torch.int16), out.cpu().view(torch.int16))
+
+    sweep = {}
+    if args.sweep:
+        for name in WORKLOADS:
+            if name == args.workload:
+                continue
+            sweep[name] = sweep_point(name, args, dev)
+    return dict(us_launch=us_launch_max, ms_per_step=ms_per_step, algo_bytes=algo_bytes,
+                distinct=distinct, clocks=clk.summary(), err=err, e2e_us=e2e_us,
+                h2d=xh.numel() * 2 + ih.numel() * 4 + wh.numel() * 4, d2h=oh.numel() * 2,
+                sweep=sweep, T=shape.T)
+
+
+def sweep_point(name, args, dev):
+    """us per launch for another workload (same protocol, fewer steps)."""
+    import torch
+
+    from moe_layer_decode_persistent_b300 import binding as B
+    from moe_layer_decode_persistent_b300 import inputs
+    wl = WORKLOADS[name]
+    shape = inputs.dsv3(wl["T"])
+    L = inputs.make_layer(shape, wl["routing"], 0, dev, inputs.FMT_NVFP4, inputs.FMT_FP8_B128)
+    copies = [(L.routed, L.shared)] + [
+        (inputs.ExpertSet(**{k: (v.clone() if isinstance(v, torch.Tensor) else v)
+                             for k, v in L.routed.__dict__.items()}), L.shared)
+        for _ in range(N_COPIES - 1)]
+    weights = [(B.make_weights(r), B.make_weights(s)) for r, s in copies]
+    sh = B.make_shape(shape.T, shape.H, shape.I, shape.I_shared, shape.E, shape.K, args.flags)
+    ws = torch.empty(B.moe_workspace_bytes(sh), dtype=torch.uint8, device=dev)
+    B.moe_workspace_init(ws)
+    out = torch.empty(shape.T, shape.H, dtype=torch.bfloat16, device=dev)
+    for i in range(3):
+        B.moe_fused_decode(L.x, L.topk_ids, L.topk_w, *weights[i % N_COPIES], out, sh, ws)
+    n = max(10, args.steps // 2)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    torch.cuda.synchronize()
+    for i in range(n):
+        ev[i][0].record()
+        B.moe_fused_decode(L.x, L.topk_ids, L.topk_w, *weights[i % N_COPIES], out, sh, ws)
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    assert B.moe_read_error(ws) == 0
+    us = statistics.mean(a.elapsed_time(b) * 1e3 for a, b in ev)
+    b, distinct = algorithmic_bytes(L, L.topk_ids.cpu())
+    peak, _ = measured_peaks()
+    gbs = b / (us * 1e-6) / 1e9
+    del L, copies, weights
+    torch.cuda.empty_cache()
+    return {"us_per_launch": round(us, 2), "hbm_gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+            "distinct_experts": distinct, "algo_bytes": b}
+
+
+def oracle_sample(workload: str, n_experts_per_step: int = 1):
+    """A bounded sample of the workload for the CPU oracle: the first rows'
+    expert uses (expert FFNs), and the scale factor to a whole layer launch."""
+    import numpy as np
+
+    import oracle
+    from moe_layer_decode_persistent_b300 import inputs
+    wl = WORKLOADS[workload]
+    shape = inputs.dsv3(wl["T"])
+    ids = inputs.ROUTINGS[wl["routing"]](shape.T, shape.K, shape.E, 0).numpy()
+    e = int(ids[0, 0])
+    routed = inputs.make_experts(inputs.FMT_NVFP4, 1, shape.H, shape.I, ("L", 0, 0), "cpu",
+                                 tag="routed")  # one expert's bytes stand in for expert e
+    ws = oracle.WeightSet(routed.fmt, routed.w13, routed.w2, routed.w13_scale, routed.w2_scale,
+                          routed.w13_gscale, routed.w2_gscale)
+    x = inputs.activations(1, shape.H, 0).double().numpy()[0]
+    uses = shape.T * shape.K + shape.T  # expert FFN evaluations in one layer launch
+    return (lambda: oracle.expert_ffn(ws, shape.H, shape.I, 0, x)), uses, e
+
+
+def run_reference(args, rank, world):
+    import oracle
+    oracle.build()
+    fn, uses, _ = oracle_sample(args.workload)
+    for _ in range(max(1, min(args.warmup, 1))):
+        fn()
+    times = []
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        fn()
+        times.append(time.perf_counter() - t)
+    per_ffn = statistics.mean(times)
+    us_layer = per_ffn * uses * 1e6
+    return us_layer, per_ffn, uses
+
+
+def cpu_baseline(args):
+    """The oracle as it stands, timed on this host on a bounded sample."""
+    import oracle
+    oracle.build()
+    fn, uses, _ = oracle_sample(args.workload)
+    t = time.perf_counter()
+    n = 0
+    while n < 3 or time.perf_counter() - t < 8.0:
+        fn()
+        n += 1
+    per_ffn = (time.perf_counter() - t) / n
+    return {"value": round(per_ffn * uses * 1e6, 1), "unit": "us", "cores": 1, "kind": "oracle",
+            "sample": f"{n} single-row expert FFNs (dequant + SwiGLU + down, fp64) of one NVFP4 "
+                      f"DSv3 expert, scaled by the {uses} expert uses of one {args.workload} "
+                      f"launch; the oracle is single-threaded per row"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=list(WORKLOADS), default="dsv3_t1")
+    ap.add_argument("--flags", type=int, default=0)
+    ap.add_argument("--sweep", action="store_true", help="also time the T=8 and T=64 workloads")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank, world, local = dist_setup(args)
+    T = WORKLOADS[args.workload]["T"]
+    metric = "us per MoE-layer launch"
+    config = {"workload": f"{args.workload}: DeepSeek-V3-shaped decode MoE layer, T={T}, H=7168, "
+                          f"routed I=2048 NVFP4 E=256 top-8, shared I=2048 FP8 128x128, "
+                          f"{WORKLOADS[args.workload]['routing']} routing",
+              "T": T, "l2": f"{N_COPIES} resident weight copies rotated per step (inputs larger than L2)"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        us_layer, per_ffn, uses = run_reference(args, rank, world)
+        line = {"impl": "reference", "metric": metric, "value": round(us_layer, 1), "unit": "us",
+                "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": round(us_layer / 1e3, 3), "higher_is_better": False,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": config,
+                "cpu_baseline": {"value": round(us_layer, 1), "unit": "us", "cores": 1,
+                                 "kind": "oracle",
+                                 "sample": f"per step one single-row NVFP4 expert FFN in fp64, "
+                                           f"scaled by the {uses} expert uses of a launch"},
+                "e2e": {"value": round(us_layer, 1), "unit": "us", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    r = run_ours(args, rank, world, local)
+    if rank != 0:
+        return
+    peak, peak_kind = measured_peaks()
+    gbs = r["algo_bytes"] / (r["us_launch"] * 1e-6) / 1e9
+    trec = traffic_record("fused_fma_kernel")
+    line = {
+        "metric": metric, "value": round(r["us_launch"], 2), "unit": "us", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(r["ms_per_step"], 4),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "fp32",
+        "data": "synthetic (seeded N(0,0.02) weights encoded to NVFP4/FP8, bf16 N(0,1) x)",
+        "config": config,
+        "hbm_gbs": round(gbs, 1), "distinct_experts": r["distinct"], "algo_bytes": r["algo_bytes"],
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(gbs / peak, 4), "peak_kind": peak_kind,
+                     "traffic": (trec or {}).get("dram_bytes_per_launch"),
+                     "kernel": "fused_fma_kernel"},
+        "e2e": {"value": round(r["e2e_us"], 2), "unit": "us", "h2d_bytes_per_step": r["h2d"],
+                "d2h_bytes_per_step": r["d2h"]},
+        "gpu_launches": args.steps, "clocks": r["clocks"], "device_error_word": r["err"],
+    }
+    if r["sweep"]:
+        line["sweep"] = r["sweep"]
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args)
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -215,36 +215,40 @@ class ExpertSet:
 
 
 def make_experts(fmt: int, E: int, H: int, I: int, seed, device="cpu", std: float = 0.02,
-                 tag: str = "routed") -> ExpertSet:
-    """E SwiGLU experts, each drawn from its own seed (so a subset regenerates alike)."""
+                 tag: str = "routed", only=None) -> ExpertSet:
+    """E SwiGLU experts, each drawn from its own seed (so a subset regenerates alike).
+
+    only: if given, just those experts are drawn and the rest stay zero (tests
+    that touch a few experts of a large set use it to save time)."""
+    todo = range(E) if only is None else sorted(set(int(e) for e in only))
     if fmt == FMT_BF16:
-        w13 = torch.empty(E, 2 * I, H, dtype=torch.bfloat16, device=device)
-        w2 = torch.empty(E, H, I, dtype=torch.bfloat16, device=device)
-        for e in range(E):
+        w13 = torch.zeros(E, 2 * I, H, dtype=torch.bfloat16, device=device)
+        w2 = torch.zeros(E, H, I, dtype=torch.bfloat16, device=device)
+        for e in todo:
             g = _gen(device, tag, seed, e, "w13")
             w13[e] = (torch.randn(2 * I, H, generator=g, device=device) * std).to(torch.bfloat16)
             g = _gen(device, tag, seed, e, "w2")
             w2[e] = (torch.randn(H, I, generator=g, device=device) * std).to(torch.bfloat16)
         return ExpertSet(fmt, E, H, I, w13, w2)
     if fmt == FMT_NVFP4:
-        w13 = torch.empty(E, 2 * I, H // 2, dtype=torch.uint8, device=device)
-        s13 = torch.empty(E, 2 * I, H // 16, dtype=torch.uint8, device=device)
-        g13 = torch.empty(E, dtype=torch.float32, device=device)
-        w2 = torch.empty(E, H, I // 2, dtype=torch.uint8, device=device)
-        s2 = torch.empty(E, H, I // 16, dtype=torch.uint8, device=device)
-        g2 = torch.empty(E, dtype=torch.float32, device=device)
-        for e in range(E):
+        w13 = torch.zeros(E, 2 * I, H // 2, dtype=torch.uint8, device=device)
+        s13 = torch.zeros(E, 2 * I, H // 16, dtype=torch.uint8, device=device)
+        g13 = torch.zeros(E, dtype=torch.float32, device=device)
+        w2 = torch.zeros(E, H, I // 2, dtype=torch.uint8, device=device)
+        s2 = torch.zeros(E, H, I // 16, dtype=torch.uint8, device=device)
+        g2 = torch.zeros(E, dtype=torch.float32, device=device)
+        for e in todo:
             g = _gen(device, tag, seed, e, "w13")
             w13[e], s13[e], g13[e] = encode_nvfp4(torch.randn(2 * I, H, generator=g, device=device) * std)
             g = _gen(device, tag, seed, e, "w2")
             w2[e], s2[e], g2[e] = encode_nvfp4(torch.randn(H, I, generator=g, device=device) * std)
         return ExpertSet(fmt, E, H, I, w13, w2, s13, s2, g13, g2)
     if fmt == FMT_FP8_B128:
-        w13 = torch.empty(E, 2 * I, H, dtype=torch.uint8, device=device)
-        s13 = torch.empty(E, 2 * I // 128, H // 128, dtype=torch.float32, device=device)
-        w2 = torch.empty(E, H, I, dtype=torch.uint8, device=device)
-        s2 = torch.empty(E, H // 128, I // 128, dtype=torch.float32, device=device)
-        for e in range(E):
+        w13 = torch.zeros(E, 2 * I, H, dtype=torch.uint8, device=device)
+        s13 = torch.ones(E, 2 * I // 128, H // 128, dtype=torch.float32, device=device)
+        w2 = torch.zeros(E, H, I, dtype=torch.uint8, device=device)
+        s2 = torch.ones(E, H // 128, I // 128, dtype=torch.float32, device=device)
+        for e in todo:
             g = _gen(device, tag, seed, e, "w13")
             w13[e], s13[e] = encode_fp8_b128(torch.randn(2 * I, H, generator=g, device=device) * std)
             g = _gen(device, tag, seed, e, "w2")
@@ -265,13 +269,17 @@ class Layer:
 
 def make_layer(shape: Shape, routing: str = "uniform", seed: int = 0, device="cpu",
                fmt_routed: int = FMT_NVFP4, fmt_shared: int = FMT_FP8_B128,
-               layer: int = 0) -> Layer:
-    """One layer's weights and one batch of inputs. `layer` varies the weights only."""
+               layer: int = 0, used_only: bool = False) -> Layer:
+    """One layer's weights and one batch of inputs. `layer` varies the weights only.
+
+    used_only: draw only the routed experts this batch picks (others zero)."""
     s = shape
     ids = ROUTINGS[routing](s.T, s.K, s.E, seed)
     w = router_weights(s.T, s.K, seed)
     x = activations(s.T, s.H, seed, device)
-    routed = make_experts(fmt_routed, s.E, s.H, s.I, ("L", layer, seed), device, tag="routed")
+    only = ids.reshape(-1).tolist() if used_only else None
+    routed = make_experts(fmt_routed, s.E, s.H, s.I, ("L", layer, seed), device, tag="routed",
+                          only=only)
     shared = make_experts(fmt_shared, 1, s.H, s.I_shared, ("L", layer, seed), device, tag="shared")
     return Layer(s, x, ids.to(device), w.to(device), routed, shared)
 

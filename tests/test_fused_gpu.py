@@ -1,0 +1,219 @@
+"""The fused layer on the GPU (through the C ABI) against the fp64 oracle,
+plus the invariants the method promises: dedup bitwise equal to the one-row
+form, determinism, duplicate rows, row permutation, negative controls,
+device error bits and the bounded waits."""
+import numpy as np
+import pytest
+import torch
+
+from moe_layer_decode_persistent_b300 import binding as B
+from moe_layer_decode_persistent_b300 import inputs
+
+from gpu_util import (assert_parity, layer, oracle_ref, run_fused, shape_of, workspace)
+
+pytestmark = pytest.mark.gpu
+
+PATHS = {"fma": B.MOE_FLAG_FORCE_FMA, "auto": 0}
+
+SMALL = inputs.Shape(T=5, H=512, I=256, I_shared=384, E=16, K=4)
+FORMATS = {"nvfp4/fp8": (inputs.FMT_NVFP4, inputs.FMT_FP8_B128),
+           "fp8/nvfp4": (inputs.FMT_FP8_B128, inputs.FMT_NVFP4),
+           "bf16/bf16": (inputs.FMT_BF16, inputs.FMT_BF16)}
+
+
+@pytest.mark.parametrize("path", list(PATHS))
+def test_tiny_bf16_layer(path):
+    L = inputs.make_tiny(0, "cuda")
+    out = run_fused(L, PATHS[path])
+    assert_parity(out, oracle_ref(L))
+
+
+@pytest.mark.parametrize("path", list(PATHS))
+@pytest.mark.parametrize("fmt", list(FORMATS))
+@pytest.mark.parametrize("T", [1, 3, 5, 13])
+def test_small_layers_all_formats(path, fmt, T):
+    s = inputs.Shape(T=T, H=SMALL.H, I=SMALL.I, I_shared=SMALL.I_shared, E=SMALL.E, K=SMALL.K)
+    L = layer(s, "zipf", seed=T, fr=FORMATS[fmt][0], fs=FORMATS[fmt][1], used_only=False)
+    out = run_fused(L, PATHS[path])
+    assert_parity(out, oracle_ref(L))
+
+
+@pytest.mark.parametrize("path", list(PATHS))
+def test_non_power_of_two_k(path):
+    s = inputs.Shape(T=7, H=256, I=128, I_shared=256, E=12, K=6)
+    L = layer(s, "mtp", seed=1, used_only=False)
+    assert_parity(run_fused(L, PATHS[path]), oracle_ref(L))
+
+
+@pytest.mark.parametrize("path", list(PATHS))
+def test_dsv3_t1_uniform_full(path):
+    L = layer(inputs.dsv3(1), "uniform", seed=0)
+    assert_parity(run_fused(L, PATHS[path]), oracle_ref(L))
+
+
+@pytest.mark.parametrize("path", list(PATHS))
+def test_dsv3_t8_mtp_full(path):
+    L = layer(inputs.dsv3(8), "mtp", seed=0)
+    assert_parity(run_fused(L, PATHS[path]), oracle_ref(L))
+
+
+@pytest.mark.parametrize("path", list(PATHS))
+def test_dsv3_t64_zipf_sampled_rows(path):
+    L = layer(inputs.dsv3(64), "zipf", seed=0)
+    rows = [0, 17, 38, 63]
+    out = run_fused(L, PATHS[path])
+    assert_parity(out, oracle_ref(L, rows=rows), rows=rows)
+    assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.parametrize("path", list(PATHS))
+@pytest.mark.parametrize("case", ["small_zipf_T13", "dsv3_T8_mtp", "dsv3_T64_zipf"])
+def test_dedup_is_bitwise_equal_to_one_row_form(path, case):
+    if case == "small_zipf_T13":
+        s = inputs.Shape(T=13, H=512, I=256, I_shared=384, E=16, K=4)
+        L = layer(s, "zipf", seed=2, used_only=False)
+    elif case == "dsv3_T8_mtp":
+        L = layer(inputs.dsv3(8), "mtp", seed=1)
+    else:
+        L = layer(inputs.dsv3(64), "zipf", seed=1)
+    a = run_fused(L, PATHS[path])
+    b = run_fused(L, PATHS[path] | B.MOE_FLAG_NO_DEDUP)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+@pytest.mark.parametrize("path", list(PATHS))
+def test_repeat_launches_are_identical(path):
+    L = layer(inputs.dsv3(8), "mtp", seed=3)
+    ws = workspace(L)
+    a = run_fused(L, PATHS[path], ws=ws)
+    for _ in range(3):
+        b = run_fused(L, PATHS[path], ws=ws)
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+@pytest.mark.parametrize("path", list(PATHS))
+def test_duplicate_rows_and_permutation(path):
+    s = inputs.Shape(T=9, H=512, I=256, I_shared=384, E=16, K=4)
+    L = layer(s, "uniform", seed=4, used_only=False)
+    L.x[5] = L.x[2]
+    L.topk_ids[5] = L.topk_ids[2]
+    L.topk_w[5] = L.topk_w[2]
+    out = run_fused(L, PATHS[path])
+    assert torch.equal(out[5].view(torch.int16), out[2].view(torch.int16))
+    perm = torch.randperm(9, generator=torch.Generator().manual_seed(0)).cuda()
+    L.x, L.topk_ids, L.topk_w = L.x[perm].contiguous(), L.topk_ids[perm].contiguous(), \
+        L.topk_w[perm].contiguous()
+    out2 = run_fused(L, PATHS[path])
+    assert torch.equal(out2.view(torch.int16), out[perm].view(torch.int16))
+
+
+@pytest.mark.parametrize("path", list(PATHS))
+def test_negative_controls(path):
+    """Each perturbation changes exactly the outputs that depend on it."""
+    s = inputs.Shape(T=6, H=512, I=256, I_shared=384, E=16, K=4)
+    L = layer(s, "uniform", seed=5, used_only=False)
+    base = run_fused(L, PATHS[path]).view(torch.int16).clone()
+
+    def rows_changed(out):
+        return set(torch.nonzero((out.view(torch.int16) != base).any(dim=1)).flatten().tolist())
+
+    # one activation value negated: only its row
+    L.x[3, 100] = -L.x[3, 100]
+    assert rows_changed(run_fused(L, PATHS[path])) == {3}
+    L.x[3, 100] = -L.x[3, 100]
+    # one down-weight row of a routed expert that only some rows use
+    e = int(L.topk_ids[0, 0])
+    users = {t for t in range(s.T) if e in L.topk_ids[t].tolist()}
+    L.routed.w2[e, 7] ^= 0x77
+    assert rows_changed(run_fused(L, PATHS[path])) == users
+    L.routed.w2[e, 7] ^= 0x77
+    # the shared expert zeroed: every row (the silently dropped shared expert)
+    saved = L.shared.w2.clone()
+    L.shared.w2.zero_()
+    assert rows_changed(run_fused(L, PATHS[path])) == set(range(s.T))
+    L.shared.w2.copy_(saved)
+    assert rows_changed(run_fused(L, PATHS[path])) == set()
+
+
+@pytest.mark.parametrize("path", list(PATHS))
+def test_zero_down_weights_give_residual(path):
+    s = inputs.Shape(T=4, H=256, I=128, I_shared=128, E=8, K=2)
+    L = layer(s, "uniform", seed=6, used_only=False)
+    L.routed.w2.zero_()
+    L.shared.w2.zero_()
+    out = run_fused(L, PATHS[path])
+    assert torch.equal(out.view(torch.int16), L.x.view(torch.int16))
+
+
+def test_bad_and_repeated_ids_set_error_bits():
+    s = inputs.Shape(T=4, H=256, I=128, I_shared=128, E=8, K=2)
+    L = layer(s, "uniform", seed=7, used_only=False)
+    ref_ok = oracle_ref(L)
+    L.topk_ids[1, 1] = 99
+    ws = workspace(L)
+    out = run_fused(L, 0, ws=ws, check_err=False)
+    assert B.moe_read_error(ws) == B.MOE_DEV_BAD_EXPERT
+    ref = oracle_ref(L)
+    assert_parity(out, ref)
+    assert not np.array_equal(ref[1], ref_ok[1])
+    L.topk_ids[1, 1] = L.topk_ids[1, 0]
+    out = run_fused(L, 0, ws=ws, check_err=False)
+    assert B.moe_read_error(ws) == B.MOE_DEV_DUP_EXPERT
+    assert_parity(out, oracle_ref(L))
+
+
+def test_dropped_arrival_times_out_and_workspace_recovers():
+    """Fault injection on the host side of the protocol: one CTA skips an
+    arrival, every wait runs out after its budget and sets the timeout bit;
+    the context stays usable and a re-initialised workspace works again."""
+    s = inputs.Shape(T=2, H=256, I=128, I_shared=128, E=8, K=2)
+    L = layer(s, "uniform", seed=8, used_only=False)
+    ws = workspace(L)
+    run_fused(L, B.MOE_FLAG_DEBUG_DROP_ARRIVE, ws=ws, check_err=False)
+    assert B.moe_read_error(ws) & B.MOE_DEV_WAIT_TIMEOUT
+    B.moe_workspace_init(ws)
+    out = run_fused(L, 0, ws=ws)
+    assert_parity(out, oracle_ref(L))
+
+
+def test_host_buffer_entry_matches_device_entry():
+    L = layer(inputs.dsv3(8), "mtp", seed=9)
+    dev = run_fused(L, 0)
+    ws = workspace(L, host=True)
+    xh = L.x.cpu().pin_memory()
+    ih = L.topk_ids.cpu().pin_memory()
+    wh = L.topk_w.cpu().pin_memory()
+    oh = torch.empty_like(xh).pin_memory()
+    B.moe_fused_decode_host(xh, ih, wh, B.make_weights(L.routed), B.make_weights(L.shared), oh,
+                            shape_of(L), ws)
+    assert torch.equal(oh.view(torch.int16), dev.cpu().view(torch.int16))
+    assert B.moe_read_error(ws) == 0
+
+
+def test_cuda_graph_replay_equals_eager():
+    L = layer(inputs.dsv3(8), "mtp", seed=10)
+    eager = run_fused(L, 0)
+    ws = workspace(L)
+    out = torch.empty_like(eager)
+    rw, sw, sh = B.make_weights(L.routed), B.make_weights(L.shared), shape_of(L)
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        B.moe_fused_decode(L.x, L.topk_ids, L.topk_w, rw, sw, out, sh, ws)  # warm up (attributes)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        B.moe_fused_decode(L.x, L.topk_ids, L.topk_w, rw, sw, out, sh, ws)
+    out.zero_()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+    assert B.moe_read_error(ws) == 0
+
+
+def test_zero_rows_launches_nothing():
+    L = inputs.make_tiny(0, "cuda")
+    sh = B.make_shape(0, 256, 128, 128, 8, 2, 0)
+    ws = workspace(L)
+    B.moe_fused_decode(None, None, None, B.make_weights(L.routed), B.make_weights(L.shared), None, sh, ws)
+    assert B.moe_read_error(ws) == 0
