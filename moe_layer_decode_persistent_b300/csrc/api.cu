@@ -153,12 +153,16 @@ moe_status dev_info(DevInfo *out) {
 
 template <typename Kern>
 moe_status set_smem(Kern k, size_t smem, const DevInfo &d) {
-    if (smem > (size_t)d.max_smem_optin)
-        return fail(MOE_ERR_UNSUPPORTED, "needs %zu B shared memory, the device allows %d", smem,
-                    d.max_smem_optin);
-    // always the device maximum, so an attribute set for one size never
-    // undercuts a later, larger launch of the same kernel
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, d.max_smem_optin);
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, k);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncGetAttributes");
+    const size_t limit = (size_t)d.max_smem_optin - fa.sharedSizeBytes;
+    if (smem > limit)
+        return fail(MOE_ERR_UNSUPPORTED, "needs %zu B dynamic shared memory, the device allows %zu",
+                    smem, limit);
+    // always the largest allowed size, so an attribute set for one launch
+    // never undercuts a later, larger launch of the same kernel
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)limit);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
     return MOE_OK;
 }

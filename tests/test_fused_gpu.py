@@ -121,12 +121,13 @@ def test_negative_controls(path):
     L.x[3, 100] = -L.x[3, 100]
     assert rows_changed(run_fused(L, PATHS[path])) == {3}
     L.x[3, 100] = -L.x[3, 100]
-    # one down-weight row of a routed expert that only some rows use
+    # the down tensor scale of a routed expert that only some rows use
     e = int(L.topk_ids[0, 0])
     users = {t for t in range(s.T) if e in L.topk_ids[t].tolist()}
-    L.routed.w2[e, 7] ^= 0x77
+    assert users != set(range(s.T))
+    L.routed.w2_gscale[e] *= 4.0
     assert rows_changed(run_fused(L, PATHS[path])) == users
-    L.routed.w2[e, 7] ^= 0x77
+    L.routed.w2_gscale[e] /= 4.0
     # the shared expert zeroed: every row (the silently dropped shared expert)
     saved = L.shared.w2.clone()
     L.shared.w2.zero_()
