@@ -188,6 +188,34 @@ moe_status moe_fused_decode_host(const void *x_host, const int32_t *ids_host,
                                  const moe_shape *s, void *workspace,
                                  size_t workspace_bytes, void *stream);
 
+/*
+ * The fused layer for callers that cannot allocate device memory. The pages
+ * have no counterpart to this entry point; it exists for callers that may not
+ * call cudaMalloc: code that runs while a CUDA graph is being captured in
+ * global mode (cudaMalloc is not permitted then), plugins whose host
+ * framework owns every device allocation, and latency-critical paths that
+ * cannot take cudaMalloc's implicit device-wide synchronisation.
+ *
+ * Same computation and arguments as moe_fused_decode, minus the workspace:
+ * the scratch is a file-scope device array of 8 MiB inside the library, which
+ * every GPU that loads the library holds until the process exits. Shapes
+ * whose workspace (moe_workspace_bytes) exceeds 8 MiB are rejected with
+ * MOE_ERR_WORKSPACE before anything is launched (DeepSeek-V3 shapes: T <= 24).
+ *   err_out  optional device uint32: receives the call's device error word
+ *            (MOE_DEV_* bits); NULL to ignore it.
+ * The first call on a device looks up the array's device address there (with
+ * that device current); make that first call before any stream capture.
+ * All calls share the one array and it keeps the last call's contents; each
+ * call leaves its header cleared for the next. Calls that overlap on the GPU
+ * (different streams, or threads) race on it: serialise them. This entry
+ * point calls no cudaMalloc or cudaFree.
+ */
+moe_status moe_fused_decode_noalloc(const void *x, const int32_t *topk_ids,
+                                    const float *topk_w, const moe_weights *routed,
+                                    const moe_weights *shared, void *out,
+                                    const moe_shape *s, uint32_t *err_out,
+                                    void *stream);
+
 /* Synchronise `stream`, copy the device error word to *err_bits and clear it. */
 moe_status moe_read_error(void *workspace, uint32_t *err_bits, void *stream);
 

@@ -21,7 +21,8 @@ MOE_W_BF16, MOE_W_NVFP4, MOE_W_FP8_B128 = 0, 1, 2
 # every symbol include/moe.h declares
 EXPORTS = ("moe_workspace_bytes", "moe_workspace_bytes_host", "moe_workspace_init",
            "moe_group_table_ints", "moe_group_table", "moe_fused_decode", "moe_fused_decode_host",
-           "moe_read_error", "moe_status_string", "moe_last_error_detail")
+           "moe_fused_decode_noalloc", "moe_read_error", "moe_status_string",
+           "moe_last_error_detail")
 
 
 class moe_weights(ctypes.Structure):
@@ -69,6 +70,8 @@ def lib():
         L.moe_fused_decode.argtypes = [P, P, P, wp, wp, P, sp, P, S, P]
         L.moe_fused_decode_host.restype = I
         L.moe_fused_decode_host.argtypes = [P, P, P, wp, wp, P, sp, P, S, P]
+        L.moe_fused_decode_noalloc.restype = I
+        L.moe_fused_decode_noalloc.argtypes = [P, P, P, wp, wp, P, sp, P, P]
         L.moe_read_error.restype = I
         L.moe_read_error.argtypes = [P, ctypes.POINTER(U), P]
         L.moe_status_string.restype = ctypes.c_char_p
@@ -153,6 +156,15 @@ def moe_fused_decode_host(x_host, ids_host, w_host, routed: moe_weights, shared:
                                      ctypes.byref(routed), ctypes.byref(shared), _ptr(out_host),
                                      ctypes.byref(shape), _ptr(ws), ws.numel() * ws.element_size(),
                                      _stream(stream))
+    return _check(st) if check else st
+
+
+def moe_fused_decode_noalloc(x, topk_ids, topk_w, routed: moe_weights, shared: moe_weights, out,
+                             shape: moe_shape, err_out=None, stream=None, check=True):
+    """The layer with the library's built-in scratch (no workspace, no allocation)."""
+    st = lib().moe_fused_decode_noalloc(_ptr(x), _ptr(topk_ids), _ptr(topk_w), ctypes.byref(routed),
+                                        ctypes.byref(shared), _ptr(out), ctypes.byref(shape),
+                                        _ptr(err_out), _stream(stream))
     return _check(st) if check else st
 
 

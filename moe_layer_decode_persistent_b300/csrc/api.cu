@@ -269,6 +269,43 @@ moe_status fused_decode_impl(const void *x, const int32_t *ids, const float *w,
 
 }  // namespace
 
+// ---- entry point for callers that cannot allocate device memory ----------
+// Its scratch is this file-scope device array instead of a caller workspace.
+// Every GPU that loads the library holds it until the process exits. Device
+// code could name it directly; host code only ever passes the address that
+// cudaGetSymbolAddress returns for the current device (the array's name in
+// host code is a host-side stand-in, not a device address).
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // 8 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void *g_noalloc_addr[kNoAllocMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device; looked up once
+// per device, with that device current, on its first call.
+moe_status noalloc_scratch(void **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kNoAllocMaxDevices)
+        return fail(MOE_ERR_UNSUPPORTED, "device %d: the no-allocation entry handles devices 0..%d",
+                    dev, kNoAllocMaxDevices - 1);
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(no-allocation scratch)");
+        g_noalloc_addr[dev] = p;
+    }
+    *out = g_noalloc_addr[dev];
+    return MOE_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 size_t moe_workspace_bytes(const moe_shape *s) {
@@ -355,6 +392,37 @@ moe_status moe_fused_decode_host(const void *x_host, const int32_t *ids_host, co
     if ((e = cudaMemcpyAsync(out_host, ws + L.st_out, xb, cudaMemcpyDeviceToHost, cs)) != cudaSuccess)
         return cuda_fail(e, "copy out to host");
     if ((e = cudaStreamSynchronize(cs)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    return MOE_OK;
+}
+
+moe_status moe_fused_decode_noalloc(const void *x, const int32_t *topk_ids, const float *topk_w,
+                                    const moe_weights *routed, const moe_weights *shared,
+                                    void *out, const moe_shape *s, uint32_t *err_out,
+                                    void *stream) {
+    moe_status st = check_shape(s);
+    if (st != MOE_OK) return st;
+    const size_t need = ws_layout(s).dev_total;
+    if (need > kNoAllocScratchBytes)
+        return fail(MOE_ERR_WORKSPACE,
+                    "this shape needs %zu B of scratch; the no-allocation entry's built-in "
+                    "scratch holds %zu B (use moe_fused_decode with a workspace)",
+                    need, kNoAllocScratchBytes);
+    if (err_out && !aligned(err_out, 4)) return fail(MOE_ERR_INVALID_ARG, "err_out not 4-byte aligned");
+    void *scratch = nullptr;
+    if ((st = noalloc_scratch(&scratch)) != MOE_OK) return st;
+    cudaStream_t cs = (cudaStream_t)stream;
+    // The header must be zero when the kernel starts. The array is zero when
+    // the library loads, and every call below leaves it zero again.
+    st = fused_decode_impl(x, topk_ids, topk_w, routed, shared, out, s, scratch,
+                           kNoAllocScratchBytes, cs);
+    if (st != MOE_OK) return st;
+    cudaError_t e;
+    if (err_out &&
+        (e = cudaMemcpyAsync(err_out, scratch, sizeof(uint32_t), cudaMemcpyDeviceToDevice, cs)) !=
+            cudaSuccess)
+        return cuda_fail(e, "copy error word");
+    if ((e = cudaMemsetAsync(scratch, 0, sizeof(moe::WsHeader), cs)) != cudaSuccess)
+        return cuda_fail(e, "clear no-allocation scratch header");
     return MOE_OK;
 }
 
