@@ -196,11 +196,14 @@ moe_status moe_fused_decode_host(const void *x_host, const int32_t *ids_host,
  * framework owns every device allocation, and latency-critical paths that
  * cannot take cudaMalloc's implicit device-wide synchronisation.
  *
- * Same computation and arguments as moe_fused_decode, minus the workspace:
- * the scratch is a file-scope device array of 8 MiB inside the library, which
+ * Same computation and arguments as moe_fused_decode, minus the workspace,
+ * always on the CUDA-core contraction (MOE_FLAG_FORCE_FMA; its fp32
+ * intermediates are the smaller scratch): the scratch is a file-scope device
+ * array of 8 MiB inside the library, which
  * every GPU that loads the library holds until the process exits. Shapes
- * whose workspace (moe_workspace_bytes) exceeds 8 MiB are rejected with
- * MOE_ERR_WORKSPACE before anything is launched (DeepSeek-V3 shapes: T <= 24).
+ * whose CUDA-core scratch, 256 + 4*T*(K+1)*(max(I, I_shared) + H) bytes,
+ * exceeds 8 MiB are rejected with MOE_ERR_WORKSPACE before anything is
+ * launched (DeepSeek-V3 shapes: T <= 24).
  *   err_out  optional device uint32: receives the call's device error word
  *            (MOE_DEV_* bits); NULL to ignore it.
  * The first call on a device looks up the array's device address there (with

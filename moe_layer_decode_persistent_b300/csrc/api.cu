@@ -12,6 +12,7 @@
 
 #include "../../include/moe.h"
 #include "fused_fma.cuh"
+#include "fused_tc.cuh"
 
 namespace {
 
@@ -35,9 +36,16 @@ constexpr int kMaxT = 256, kMaxK = 16, kMaxE = 1024, kMaxDim = 16384;
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-// Workspace: header | mid fp32 [Ucap][Imax] | y fp32 [Ucap][H] | host staging.
+// Workspace. Both kernels share the 256-byte header (error word, counters).
+//   CUDA-core path : header | mid fp32 [Ucap][Imax] | y fp32 [Ucap][H]
+//   tensor path    : header | group_ready [C] | tile_cnt [C*Imax/128*4] |
+//                    htile_cnt [H/256*4] | P | Y | midB
+// followed by the host-buffer call's staging area. Ucap = C = T*(K+1).
 struct WsLayout {
-    size_t mid = 0, y = 0, dev_total = 0;
+    size_t mid = 0, y = 0, fma_end = 0;
+    size_t tc_ready = 0, tc_tile = 0, tc_htile = 0, tc_ctrl_end = 0, tc_P = 0, tc_Y = 0, tc_midB = 0,
+           tc_end = 0;
+    size_t dev_total = 0;
     size_t st_x = 0, st_ids = 0, st_w = 0, st_out = 0, host_total = 0;
 };
 
@@ -46,20 +54,44 @@ WsLayout ws_layout(const moe_shape *s) {
     const size_t T = (size_t)std::max(s->T, 0), K = (size_t)std::max(s->K, 0);
     const size_t Ucap = T * (K + 1);
     const size_t Imax = (size_t)std::max(s->I, s->I_shared);
+    const size_t H = (size_t)s->H;
     size_t off = sizeof(moe::WsHeader);
     L.mid = off = align_up(off, 256);
     off += Ucap * Imax * sizeof(float);
     L.y = off = align_up(off, 256);
-    off += Ucap * (size_t)s->H * sizeof(float);
-    L.dev_total = off = align_up(off, 256);
+    off += Ucap * H * sizeof(float);
+    L.fma_end = align_up(off, 256);
+
+    off = sizeof(moe::WsHeader);
+    L.tc_ready = off;
+    off += Ucap * 4;
+    L.tc_tile = off = align_up(off, 16);
+    off += Ucap * (Imax / 128) * 4 * 4;
+    L.tc_htile = off = align_up(off, 16);
+    off += ((H + 255) / 256) * 4 * 4;
+    L.tc_ctrl_end = off = align_up(off, 256);
+    const int Ti = (int)T, Hi = (int)H;
+    const size_t nkc_gu = Ti <= moe::kSplitMaxT
+                              ? (size_t)std::max(moe::tc_nkc_gu(moe::kFmtNvfp4, Hi, Ti),
+                                                 moe::tc_nkc_gu(moe::kFmtFp8B128, Hi, Ti))
+                              : 0;
+    L.tc_P = off;
+    off += nkc_gu * 2 * Ucap * Imax * sizeof(float);
+    L.tc_Y = off = align_up(off, 256);
+    off += (size_t)moe::tc_nkc_dn((int)Imax, Ti) * Ucap * H * sizeof(float);
+    L.tc_midB = off = align_up(off, 256);
+    off += 16 * Ucap * (Imax / 128) * 512;  // sum of padded column counts <= 16 * Ucap
+    L.tc_end = align_up(off, 256);
+
+    L.dev_total = off = std::max(L.fma_end, L.tc_end);
     L.st_x = off;
-    off = align_up(off + T * (size_t)s->H * 2, 256);
+    off = align_up(off + T * H * 2, 256);
     L.st_ids = off;
     off = align_up(off + T * K * 4, 256);
     L.st_w = off;
     off = align_up(off + T * K * 4, 256);
     L.st_out = off;
-    off = align_up(off + T * (size_t)s->H * 2, 256);
+    off = align_up(off + T * H * 2, 256);
     L.host_total = off;
     return L;
 }
@@ -223,6 +255,163 @@ moe_status launch_fused_fma(const moe::FusedParams &p, const moe_shape *s, cudaS
     return MOE_OK;
 }
 
+// ---- tensor maps (cached: encoding costs microseconds of host time) ----------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+
+moe_status encode_fn(EncodeTiledFn *out) {
+    static EncodeTiledFn fn = nullptr;
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!fn) {
+        cudaDriverEntryPointQueryResult q;
+        void *ptr = nullptr;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                                         cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !ptr)
+            return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+        fn = (EncodeTiledFn)ptr;
+    }
+    *out = fn;
+    return MOE_OK;
+}
+
+// 3-D uint8 map over [E][rows][cols] bytes; box [box_c][128][1].
+moe_status tensor_map(CUtensorMap *out, const void *base, size_t cols, size_t rows, size_t E, int box_c,
+                      bool swz128) {
+    struct Key {
+        const void *b;
+        size_t c, r, e;
+        int bc, sw;
+        bool operator==(const Key &o) const {
+            return b == o.b && c == o.c && r == o.r && e == o.e && bc == o.bc && sw == o.sw;
+        }
+    };
+    struct KeyHash {
+        size_t operator()(const Key &k) const {
+            return std::hash<const void *>()(k.b) ^ (k.c * 1000003u) ^ (k.r * 10007u) ^ (k.e * 101u) ^
+                   (size_t)k.bc ^ ((size_t)k.sw << 20);
+        }
+    };
+    static std::mutex mu;
+    static std::unordered_map<Key, CUtensorMap, KeyHash> cache;
+    const Key key{base, cols, rows, E, box_c, swz128 ? 1 : 0};
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) {
+            *out = it->second;
+            return MOE_OK;
+        }
+    }
+    EncodeTiledFn enc;
+    moe_status st = encode_fn(&enc);
+    if (st != MOE_OK) return st;
+    cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)E};
+    cuuint64_t strides[2] = {(cuuint64_t)cols, (cuuint64_t)(cols * rows)};
+    cuuint32_t box[3] = {(cuuint32_t)box_c, 128, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = enc(out, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     swz128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    std::lock_guard<std::mutex> lk(mu);
+    cache[key] = *out;
+    return MOE_OK;
+}
+
+// codes and (NVFP4) block-scale maps of one expert set
+moe_status set_maps(const moe_weights *w, int E, int H, int I, CUtensorMap *m13, CUtensorMap *m13s,
+                    CUtensorMap *m2, CUtensorMap *m2s) {
+    const bool fp4 = w->fmt == MOE_W_NVFP4;
+    const size_t h_b = fp4 ? (size_t)H / 2 : (size_t)H, i_b = fp4 ? (size_t)I / 2 : (size_t)I;
+    moe_status st = tensor_map(m13, w->w13, h_b, 2 * (size_t)I, E, 128, true);
+    if (st == MOE_OK) st = tensor_map(m2, w->w2, i_b, (size_t)H, E, 128, true);
+    if (st != MOE_OK) return st;
+    if (fp4) {
+        st = tensor_map(m13s, w->w13_scale, (size_t)H / 16, 2 * (size_t)I, E, 16, false);
+        if (st == MOE_OK) st = tensor_map(m2s, w->w2_scale, (size_t)I / 16, (size_t)H, E, 16, false);
+        return st;
+    }
+    *m13s = *m13;  // unused for FP8
+    *m2s = *m2;
+    return MOE_OK;
+}
+
+// Whether the tensor-core path handles this launch (and why not).
+bool tc_eligible(const moe_shape *s, const moe_weights *routed, const moe_weights *shared, const char **why) {
+    if (routed->fmt == MOE_W_BF16 || shared->fmt == MOE_W_BF16) {
+        *why = "bf16 weights use the CUDA-core path";
+        return false;
+    }
+    if (s->H % 256 || s->I % 256 || s->I_shared % 256) {
+        *why = "H, I and I_shared must be multiples of 256";
+        return false;
+    }
+    if (s->T > moe::kTcMaxT) {
+        *why = "T above 64";
+        return false;
+    }
+    return true;
+}
+
+moe_status launch_fused_tc(const moe::FusedParams &fp, const WsLayout &L, const moe_shape *s,
+                           const moe_weights *routed, const moe_weights *shared, cudaStream_t stream) {
+    DevInfo d;
+    moe_status st = dev_info(&d);
+    if (st != MOE_OK) return st;
+    moe::TcParams p;
+    memset(&p, 0, sizeof p);
+    if ((st = set_maps(routed, s->E, s->H, s->I, &p.maps.r13, &p.maps.r13s, &p.maps.r2, &p.maps.r2s)) != MOE_OK)
+        return st;
+    if ((st = set_maps(shared, 1, s->H, s->I_shared, &p.maps.s13, &p.maps.s13s, &p.maps.s2, &p.maps.s2s)) !=
+        MOE_OK)
+        return st;
+    p.x = fp.x;
+    p.ids = fp.ids;
+    p.topk_w = fp.topk_w;
+    p.routed = fp.routed;
+    p.shared = fp.shared;
+    p.out = fp.out;
+    p.T = s->T;
+    p.H = s->H;
+    p.I = s->I;
+    p.Is = s->I_shared;
+    p.E = s->E;
+    p.K = s->K;
+    p.flags = s->flags;
+    char *ws = reinterpret_cast<char *>(fp.hdr);
+    p.hdr = fp.hdr;
+    p.group_ready = reinterpret_cast<uint32_t *>(ws + L.tc_ready);
+    p.tile_cnt = reinterpret_cast<uint32_t *>(ws + L.tc_tile);
+    p.htile_cnt = reinterpret_cast<uint32_t *>(ws + L.tc_htile);
+    p.P = reinterpret_cast<float *>(ws + L.tc_P);
+    p.Y = reinterpret_cast<float *>(ws + L.tc_Y);
+    p.midB = reinterpret_cast<uint8_t *>(ws + L.tc_midB);
+    p.Ucap = s->T * (s->K + 1);
+    p.Imax = std::max(s->I, s->I_shared);
+    const size_t smem = (size_t)moe::tc_smem_bytes(s->T, s->K);
+    int occ = 0;
+    if ((st = plan_occupancy(moe::fused_tc_kernel, moe::kTcThreads, smem, d, &occ)) != MOE_OK) return st;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)d.nsm);  // one CTA per SM: it holds all of TMEM
+    cfg.blockDim = dim3(moe::kTcThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, moe::fused_tc_kernel, p);
+    if (e != cudaSuccess) return cuda_fail(e, "launch fused_tc_kernel");
+    return MOE_OK;
+}
+
 moe_status fused_decode_impl(const void *x, const int32_t *ids, const float *w,
                              const moe_weights *routed, const moe_weights *shared, void *out,
                              const moe_shape *s, void *ws, size_t ws_bytes, cudaStream_t stream) {
@@ -233,8 +422,14 @@ moe_status fused_decode_impl(const void *x, const int32_t *ids, const float *w,
     if (!ws) return fail(MOE_ERR_INVALID_ARG, "workspace is NULL");
     if (!aligned(ws, 256)) return fail(MOE_ERR_INVALID_ARG, "workspace not 256-byte aligned");
     const WsLayout L = ws_layout(s);
-    if (ws_bytes < L.dev_total)
-        return fail(MOE_ERR_WORKSPACE, "workspace has %zu B, needs %zu B", ws_bytes, L.dev_total);
+    const char *why = "";
+    const bool tc_ok = tc_eligible(s, routed, shared, &why);
+    bool use_tc = tc_ok && !(s->flags & MOE_FLAG_FORCE_FMA);
+    if ((s->flags & MOE_FLAG_FORCE_MMA) && !tc_ok)
+        return fail(MOE_ERR_UNSUPPORTED, "tensor-core path requested but unavailable: %s", why);
+    const size_t need = use_tc ? L.tc_end : L.fma_end;
+    if (ws_bytes < need)
+        return fail(MOE_ERR_WORKSPACE, "workspace has %zu B, needs %zu B", ws_bytes, need);
     if (s->T == 0) return MOE_OK;
     if (!x || !out || !ids || !w) return fail(MOE_ERR_INVALID_ARG, "NULL x/out/topk_ids/topk_w");
     if (!aligned(x, 16) || !aligned(out, 16))
@@ -264,6 +459,7 @@ moe_status fused_decode_impl(const void *x, const int32_t *ids, const float *w,
     p.mid = reinterpret_cast<float *>(static_cast<char *>(ws) + L.mid);
     p.y = reinterpret_cast<float *>(static_cast<char *>(ws) + L.y);
     p.Imax = std::max(s->I, s->I_shared);
+    if (use_tc) return launch_fused_tc(p, L, s, routed, shared, stream);
     return launch_fused_fma(p, s, stream);
 }
 
@@ -327,7 +523,7 @@ moe_status moe_workspace_init(void *workspace, size_t workspace_bytes, void *str
     if (!workspace) return fail(MOE_ERR_INVALID_ARG, "workspace is NULL");
     if (workspace_bytes < sizeof(moe::WsHeader))
         return fail(MOE_ERR_WORKSPACE, "workspace smaller than its %zu-byte header", sizeof(moe::WsHeader));
-    cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(moe::WsHeader), (cudaStream_t)stream);
+    cudaError_t e = cudaMemsetAsync(workspace, 0, workspace_bytes, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
     return MOE_OK;
 }
@@ -401,7 +597,11 @@ moe_status moe_fused_decode_noalloc(const void *x, const int32_t *topk_ids, cons
                                     void *stream) {
     moe_status st = check_shape(s);
     if (st != MOE_OK) return st;
-    const size_t need = ws_layout(s).dev_total;
+    // the built-in scratch serves the CUDA-core contraction, whose scratch is
+    // the smaller one (the fp32 intermediates only)
+    moe_shape sf = *s;
+    sf.flags = (sf.flags & ~(unsigned)MOE_FLAG_FORCE_MMA) | MOE_FLAG_FORCE_FMA;
+    const size_t need = ws_layout(&sf).fma_end;
     if (need > kNoAllocScratchBytes)
         return fail(MOE_ERR_WORKSPACE,
                     "this shape needs %zu B of scratch; the no-allocation entry's built-in "
@@ -413,7 +613,7 @@ moe_status moe_fused_decode_noalloc(const void *x, const int32_t *topk_ids, cons
     cudaStream_t cs = (cudaStream_t)stream;
     // The header must be zero when the kernel starts. The array is zero when
     // the library loads, and every call below leaves it zero again.
-    st = fused_decode_impl(x, topk_ids, topk_w, routed, shared, out, s, scratch,
+    st = fused_decode_impl(x, topk_ids, topk_w, routed, shared, out, &sf, scratch,
                            kNoAllocScratchBytes, cs);
     if (st != MOE_OK) return st;
     cudaError_t e;

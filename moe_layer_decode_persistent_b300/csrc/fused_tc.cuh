@@ -1,0 +1,859 @@
+// fused_tc.cuh -- the fused decode MoE layer on the tcgen05 tensor cores.
+//
+// One persistent cooperative launch, one CTA per SM, computes the whole layer
+// ("Daily AI Hotspot 2026-08-21", section "Most Worth Your Attention Today":
+// shared gate/up, routed experts, shared down and the residual add in one
+// pass, FP32 accumulation, BF16 written once) over the step's deduplicated
+// groups (PR #27 "each expert once", "Motivation"/"Modifications": each
+// distinct expert streams its weights once, with every row that uses it as an
+// MMA column; jobs are the intermediate tiles of each group, dealt over the
+// CTAs; a row's output is summed in a fixed order so the dedup form is bitwise
+// equal to the one-row form).
+//
+// Work items ("jobs"), claimed in list order from one global counter:
+//   gate/up job (group g, column tile ct, 128-row tile rt, K chunk kc):
+//     tile0 = gate rows rt*128.., tile1 = up rows I+rt*128.., K = H chunk
+//   down job (g, ct, 256-row tile ht, K chunk kc):
+//     tile0 = rows ht*256.., tile1 = rows ht*256+128.., K = I chunk
+// Both tiles of a job share the B operand (the group's activation columns).
+//
+// Per CTA the roles are warp-specialised (16 warps):
+//   warp 0      producer: claims jobs, TMA-loads 128-byte-wide weight boxes
+//               (SWIZZLE_128B) and NVFP4 block scales into a 3-stage ring
+//   warp 1      MMA issuer: tcgen05.mma kind::f16, M=128, N=16|32, K=16,
+//               A from TMEM, B from shared memory; commits to mbarriers
+//   warps 2-3   B stagers: gather + convert activation columns bf16->f16
+//               (gate/up) or bulk-copy the split f16 intermediate (down)
+//   warps 4-7   dequant of tile0, warps 8-11 dequant of tile1: one thread per
+//               weight row, E2M1*E4M3 -> exact f16 (or E4M3 -> f16), written
+//               to TMEM as the MMA's A operand (the weights never touch
+//               shared memory as f16)
+//   warps 12-15 epilogue: TMEM accumulators -> registers; FP8 128x128 block
+//               scales applied per 128-K block in fp32; partial sums, the
+//               fixed-order reductions, SwiGLU, the split f16 intermediate,
+//               and the final combine + single bf16 write
+//
+// Precision: weights dequantise exactly to f16 (e2m1*e4m3 has <= 6
+// significant bits); activations bf16 -> f16 (exact for |x| in [2^-17, 65504];
+// larger magnitudes set MOE_DEV_RANGE); the fp32 SwiGLU intermediate is split
+// hi = f16(m), lo = f16(m - hi) and both halves go through the MMA; every
+// accumulation is fp32.
+#pragma once
+
+#include <cuda.h>
+
+#include "group_table.cuh"
+#include "moe_common.cuh"
+#include "sm100.cuh"
+
+namespace moe {
+
+constexpr int kTcThreads = 512;
+constexpr int kTcMaxT = 64;
+constexpr int kNt = 32;               // columns per job at most
+constexpr int kUnitK = 128;           // K elements of one TMEM A unit per tile
+constexpr int kRawStages = 3;
+constexpr int kRawTileBytes = 16384;  // 128 rows x 128 bytes
+constexpr int kRawScaleOff = 2 * kRawTileBytes;
+constexpr int kRawStageBytes = 2 * kRawTileBytes + 2 * 2048;  // + NVFP4 scales
+constexpr int kBStages = 3;
+constexpr int kBStageBytes = 2 * kNt * kUnitK * 2;  // hi + lo f16
+constexpr int kASlots = 3;
+constexpr int kJobSlots = 4;
+constexpr int kTmemCols = 512;
+constexpr int kDCol = kASlots * 128;  // two D sets of (32 + 32) columns follow
+constexpr int kKcNvfp4 = 1792;
+constexpr int kKcFp8 = 1024;
+constexpr int kKcDown = 1024;
+constexpr int kSplitMaxT = 16;
+
+struct TcMaps {
+    CUtensorMap r13, r13s, r2, r2s, s13, s13s, s2, s2s;
+};
+
+struct TcParams {
+    TcMaps maps;
+    const __nv_bfloat16 *x;
+    const int32_t *ids;
+    const float *topk_w;
+    WeightsDev routed, shared;
+    __nv_bfloat16 *out;
+    int T, H, I, Is, E, K;
+    unsigned flags;
+    WsHeader *hdr;
+    uint32_t *group_ready;  // per (group, column tile)
+    uint32_t *tile_cnt;     // per (group, column tile, 128-row tile)
+    uint32_t *htile_cnt;    // per 256-row output tile
+    float *P;               // gate/up partials [kc][2][Ucap][Imax]
+    float *Y;               // down partials [kc][Ucap][H]
+    uint8_t *midB;          // split intermediate in MMA B layout
+    int Ucap, Imax;
+};
+
+struct TcJob {
+    int kind;  // 0 gate/up, 1 down, -1 end
+    int g, ct, tile, kc, nkc;
+    int e, shared, fmt, Ig;
+    int n, npad, col0;
+    int k0, nunits;
+    int rows0, rows1;
+    int tile_id, pair;
+    long long mid_off;  // bytes into midB of this (group, column tile)
+};
+
+// ---- per-launch constants shared by host and device -----------------------
+
+__host__ __device__ inline int tc_nkc_gu(int fmt, int H, int T) {
+    if (T > kSplitMaxT) return 1;
+    const int kc = fmt == kFmtNvfp4 ? kKcNvfp4 : kKcFp8;
+    return (H + kc - 1) / kc;
+}
+__host__ __device__ inline int tc_kc_gu(int fmt, int H, int T) {
+    return T > kSplitMaxT ? H : (fmt == kFmtNvfp4 ? kKcNvfp4 : kKcFp8);
+}
+__host__ __device__ inline int tc_nkc_dn(int Ig, int T) {
+    return T > kSplitMaxT ? 1 : (Ig + kKcDown - 1) / kKcDown;
+}
+__host__ __device__ inline int tc_kc_dn(int Ig, int T) { return T > kSplitMaxT ? Ig : kKcDown; }
+
+// B-operand layout of a [n][128] f16 unit: core matrices of 8 columns x 8 K.
+__device__ __forceinline__ uint32_t b_off(int n, int k) {
+    return (uint32_t)(((n >> 3) * 16 + (k >> 3)) * 128 + (n & 7) * 16 + (k & 7) * 2);
+}
+
+// Shared-memory layout of the fused kernel (dynamic, 1024-aligned base).
+struct TcSmem {
+    static constexpr int raw = 0;
+    static constexpr int bbuf = raw + kRawStages * kRawStageBytes;  // 110592
+    static constexpr int jobs = bbuf + kBStages * kBStageBytes;      // 159744
+    static constexpr int bars = jobs + kJobSlots * (int)sizeof(TcJob);
+    // mbarriers: jfull, jempty, rfull, rempty, afull, aempty, bfull, bempty, dfull, dempty, drain
+    static constexpr int nbars = 2 * kJobSlots + 2 * kRawStages + 2 * kASlots + 2 * kBStages + 2 * 2 + 1;
+    static constexpr int misc = bars + nbars * 8;  // tmem addr, abort, flags
+    static constexpr int tables = misc + 64;       // group table, then per-group arrays
+};
+constexpr int kTcGroupArrays = 6;  // gu_prefix, dn_prefix, tile_prefix, mid_prefix, pair_prefix (+1 spare)
+
+__host__ __device__ inline int tc_smem_bytes(int T, int K) {
+    const int C = T * (K + 1);
+    return TcSmem::tables + 4 * (group_table_ints(T, K) + kTcGroupArrays * (C + 1)) + 1024;
+}
+
+__device__ __forceinline__ uint32_t pack_h2(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
+
+__device__ __forceinline__ __half2 u32_h2(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
+
+__global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_constant__ TcParams p) {
+    using namespace sm100;
+    extern __shared__ __align__(1024) uint8_t smem_raw_[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw_) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int T = p.T, K = p.K, H = p.H;
+    const bool no_dedup = (p.flags & kFlagNoDedup) != 0;
+
+    uint8_t *raw = smem + TcSmem::raw;
+    uint8_t *bbuf = smem + TcSmem::bbuf;
+    TcJob *jobs = reinterpret_cast<TcJob *>(smem + TcSmem::jobs);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + TcSmem::bars);
+    uint64_t *jfull = bars, *jempty = jfull + kJobSlots;
+    uint64_t *rfull = jempty + kJobSlots, *rempty = rfull + kRawStages;
+    uint64_t *afull = rempty + kRawStages, *aempty = afull + kASlots;
+    uint64_t *bfull = aempty + kASlots, *bempty = bfull + kBStages;
+    uint64_t *dfull = bempty + kBStages, *dempty = dfull + 2;
+    uint64_t *drain = dempty + 2;
+    uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(smem + TcSmem::misc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + TcSmem::misc + 4);
+    int *dn_per_ht_s = reinterpret_cast<int *>(smem + TcSmem::misc + 8);
+    int32_t *tbl = reinterpret_cast<int32_t *>(smem + TcSmem::tables);
+    const int C = T * (K + 1);
+    GroupTable tab{tbl, C};
+    int *gu_prefix = tbl + group_table_ints(T, K);
+    int *dn_prefix = gu_prefix + (C + 1);
+    int *tile_prefix = dn_prefix + (C + 1);
+    int *mid_prefix = tile_prefix + (C + 1);
+    int *pair_prefix = mid_prefix + (C + 1);
+    uint32_t *err = &p.hdr->err;
+
+    // ---- prologue: group table (scratch aliases the raw ring), per-group sums
+    group_table_cta(p.ids, T, K, p.E, no_dedup, tab, reinterpret_cast<int *>(raw),
+                    blockIdx.x == 0 ? err : nullptr);
+    const int G = tab.G();
+    const int32_t *gexp = tab.gexp(), *gn = tab.gncols(), *g0 = tab.gcol0(), *rcol = tab.row_col();
+    const int *crow = tab.col_row();
+    if (warp == 0) {
+        int run_gu = 0, run_dn = 0, run_tile = 0, run_mid = 0, run_pair = 0;
+        for (int base = 0; base < G; base += 32) {
+            const int g = base + lane;
+            int v_gu = 0, v_dn = 0, v_tile = 0, v_mid = 0, v_pair = 0;
+            if (g < G) {
+                const bool sh = gexp[g] < 0;
+                const int fmt = sh ? p.shared.fmt : p.routed.fmt;
+                const int Ig = sh ? p.Is : p.I;
+                const int n = gn[g], nct = (n + kNt - 1) / kNt;
+                const int tiles = Ig / 128;
+                v_pair = nct;
+                v_tile = nct * tiles;
+                v_gu = v_tile * tc_nkc_gu(fmt, H, T);
+                v_dn = nct * (H / 256) * tc_nkc_dn(Ig, T);
+                int np = 0;
+                for (int ct = 0; ct < nct; ++ct) np += ((min(kNt, n - ct * kNt) + 15) / 16) * 16;
+                v_mid = np * tiles;
+            }
+            int s_gu = v_gu, s_dn = v_dn, s_tile = v_tile, s_mid = v_mid, s_pair = v_pair;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int a = __shfl_up_sync(0xffffffffu, s_gu, o), b = __shfl_up_sync(0xffffffffu, s_dn, o),
+                          c = __shfl_up_sync(0xffffffffu, s_tile, o), d = __shfl_up_sync(0xffffffffu, s_mid, o),
+                          f = __shfl_up_sync(0xffffffffu, s_pair, o);
+                if (lane >= o) {
+                    s_gu += a;
+                    s_dn += b;
+                    s_tile += c;
+                    s_mid += d;
+                    s_pair += f;
+                }
+            }
+            if (g < G) {
+                gu_prefix[g] = run_gu + s_gu - v_gu;
+                dn_prefix[g] = run_dn + s_dn - v_dn;
+                tile_prefix[g] = run_tile + s_tile - v_tile;
+                mid_prefix[g] = run_mid + s_mid - v_mid;
+                pair_prefix[g] = run_pair + s_pair - v_pair;
+            }
+            run_gu += __shfl_sync(0xffffffffu, s_gu, 31);
+            run_dn += __shfl_sync(0xffffffffu, s_dn, 31);
+            run_tile += __shfl_sync(0xffffffffu, s_tile, 31);
+            run_mid += __shfl_sync(0xffffffffu, s_mid, 31);
+            run_pair += __shfl_sync(0xffffffffu, s_pair, 31);
+        }
+        if (lane == 0) {
+            gu_prefix[G] = run_gu;
+            dn_prefix[G] = run_dn;
+            tile_prefix[G] = run_tile;
+            mid_prefix[G] = run_mid;
+            pair_prefix[G] = run_pair;
+            for (int i = 0; i < kJobSlots; ++i) {
+                mbar_init(&jfull[i], 1);
+                mbar_init(&jempty[i], 15);
+            }
+            for (int i = 0; i < kRawStages; ++i) {
+                mbar_init(&rfull[i], 1);
+                mbar_init(&rempty[i], 8);
+            }
+            for (int i = 0; i < kASlots; ++i) {
+                mbar_init(&afull[i], 8);
+                mbar_init(&aempty[i], 1);
+            }
+            for (int i = 0; i < kBStages; ++i) {
+                mbar_init(&bfull[i], 2);
+                mbar_init(&bempty[i], 1);
+            }
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(&dfull[i], 1);
+                mbar_init(&dempty[i], 4);
+            }
+            mbar_init(drain, 1);
+            *abort_flag = 0;
+            int dph_total = 0;  // down jobs that write one 256-row output tile
+            for (int g = 0; g < G; ++g)
+                dph_total += ((gn[g] + kNt - 1) / kNt) * tc_nkc_dn(gexp[g] < 0 ? p.Is : p.I, T);
+            *dn_per_ht_s = dph_total;
+            fence_mbar_init();
+        }
+    }
+    if (warp == 1) tmem_alloc(tmem_base_s, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_base_s;
+    const int NGU = gu_prefix[G], NDN = dn_prefix[G];
+    const int njobs = NGU + NDN;
+    const int dn_per_ht = *dn_per_ht_s;
+
+    // read one job descriptor from the ring (all threads of a role)
+    auto job_at = [&](int slot) -> TcJob { return jobs[slot]; };
+
+    if (warp == 0) {
+        // ===================== producer =====================
+        if (lane == 0) {
+            int js = 0, jph = 0, rs = 0, rph = 0;
+            int cur_gu = 0, cur_dn = 0;
+            uint32_t armed = 0;  // raw stages with a TMA in flight not yet seen consumed
+            for (;;) {
+                TcJob d;
+                const int j = (int)atomicAdd(&p.hdr->job_next, 1u);
+                if (*abort_flag) d.kind = -1;
+                else if (j >= njobs) d.kind = -1;
+                else {
+                    const bool gu = j < NGU;
+                    int g, local;
+                    if (gu) {
+                        while (gu_prefix[cur_gu + 1] <= j) ++cur_gu;
+                        g = cur_gu;
+                        local = j - gu_prefix[g];
+                    } else {
+                        const int jd = j - NGU;
+                        while (dn_prefix[cur_dn + 1] <= jd) ++cur_dn;
+                        g = cur_dn;
+                        local = jd - dn_prefix[g];
+                    }
+                    const bool sh = gexp[g] < 0;
+                    d.g = g;
+                    d.shared = sh;
+                    d.e = sh ? 0 : gexp[g];
+                    d.fmt = sh ? p.shared.fmt : p.routed.fmt;
+                    d.Ig = sh ? p.Is : p.I;
+                    const int tiles = d.Ig / 128;
+                    if (gu) {
+                        d.kind = 0;
+                        d.nkc = tc_nkc_gu(d.fmt, H, T);
+                        const int per_ct = tiles * d.nkc;
+                        d.ct = local / per_ct;
+                        const int rem = local - d.ct * per_ct;
+                        d.tile = rem / d.nkc;
+                        d.kc = rem - d.tile * d.nkc;
+                        const int kc_len = tc_kc_gu(d.fmt, H, T);
+                        d.k0 = d.kc * kc_len;
+                        d.nunits = min(kc_len, H - d.k0) / kUnitK;
+                        d.rows0 = d.tile * 128;
+                        d.rows1 = d.Ig + d.tile * 128;
+                    } else {
+                        d.kind = 1;
+                        d.nkc = tc_nkc_dn(d.Ig, T);
+                        const int per_ct = (H / 256) * d.nkc;
+                        d.ct = local / per_ct;
+                        const int rem = local - d.ct * per_ct;
+                        d.tile = rem / d.nkc;
+                        d.kc = rem - d.tile * d.nkc;
+                        const int kc_len = tc_kc_dn(d.Ig, T);
+                        d.k0 = d.kc * kc_len;
+                        d.nunits = min(kc_len, d.Ig - d.k0) / kUnitK;
+                        d.rows0 = d.tile * 256;
+                        d.rows1 = d.tile * 256 + 128;
+                    }
+                    d.n = min(kNt, gn[g] - d.ct * kNt);
+                    d.npad = ((d.n + 15) / 16) * 16;
+                    d.col0 = g0[g] + d.ct * kNt;
+                    d.tile_id = tile_prefix[g] + d.ct * tiles + (d.kind == 0 ? d.tile : 0);
+                    d.pair = pair_prefix[g] + d.ct;
+                    d.mid_off = ((long long)mid_prefix[g] + (long long)d.ct * tiles * kNt) * 512ll;
+                }
+                if (!mbar_wait(&jempty[js], jph ^ 1, abort_flag, err)) break;
+                jobs[js] = d;
+                mbar_arrive(&jfull[js]);
+                if (++js == kJobSlots) {
+                    js = 0;
+                    jph ^= 1;
+                }
+                if (d.kind < 0) break;
+                // weight boxes for the job: 128-byte-wide slices of tile0 and tile1 rows
+                const CUtensorMap *mc, *ms;
+                if (d.kind == 0) {
+                    mc = d.shared ? &p.maps.s13 : &p.maps.r13;
+                    ms = d.shared ? &p.maps.s13s : &p.maps.r13s;
+                } else {
+                    mc = d.shared ? &p.maps.s2 : &p.maps.r2;
+                    ms = d.shared ? &p.maps.s2s : &p.maps.r2s;
+                }
+                const bool fp4 = d.fmt == kFmtNvfp4;
+                const int upst = fp4 ? 2 : 1;
+                const int nst = d.nunits / upst;
+                const int kb0 = fp4 ? d.k0 / 2 : d.k0;
+                bool ok = true;
+                for (int s = 0; s < nst; ++s) {
+                    if (!mbar_wait(&rempty[rs], rph ^ 1, abort_flag, err)) {
+                        ok = false;
+                        break;
+                    }
+                    armed &= ~(1u << rs);
+                    uint8_t *dst = raw + rs * kRawStageBytes;
+                    mbar_arrive_expect_tx(&rfull[rs], fp4 ? kRawStageBytes : 2 * kRawTileBytes);
+                    tma_load_3d(dst, mc, kb0 + s * 128, d.rows0, d.e, &rfull[rs]);
+                    tma_load_3d(dst + kRawTileBytes, mc, kb0 + s * 128, d.rows1, d.e, &rfull[rs]);
+                    if (fp4) {
+                        tma_load_3d(dst + kRawScaleOff, ms, d.k0 / 16 + s * 16, d.rows0, d.e, &rfull[rs]);
+                        tma_load_3d(dst + kRawScaleOff + 2048, ms, d.k0 / 16 + s * 16, d.rows1, d.e, &rfull[rs]);
+                    }
+                    armed |= 1u << rs;
+                    if (++rs == kRawStages) {
+                        rs = 0;
+                        rph ^= 1;
+                    }
+                }
+                if (!ok) break;
+            }
+            // never leave with a TMA write into shared memory still in flight
+            if (*abort_flag && armed) {
+                for (int s = 0; s < kRawStages; ++s) {
+                    if (!(armed >> s & 1u)) continue;
+                    // the phase armed last for slot s has parity rph if s < rs, else rph ^ 1
+                    const uint32_t par = (s < rs) ? (uint32_t)rph : (uint32_t)(rph ^ 1);
+                    const unsigned long long t0 = globaltimer_ns();
+                    while (!mbar_try_wait(&rfull[s], par) && globaltimer_ns() - t0 < kWaitBudgetNs) {
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ===================== MMA issuer =====================
+        if (lane == 0) {
+            int js = 0, jph = 0, as = 0, aph = 0, bs = 0, bph = 0, ds = 0, dph = 0;
+            bool issued = false;
+            for (;;) {
+                if (!mbar_wait(&jfull[js], jph, abort_flag, err)) break;
+                const TcJob d = job_at(js);
+                mbar_arrive(&jempty[js]);
+                if (++js == kJobSlots) {
+                    js = 0;
+                    jph ^= 1;
+                }
+                if (d.kind < 0) break;
+                const uint32_t idesc = idesc_f16(128, d.npad);
+                const bool fp8 = d.fmt == kFmtFp8B128;
+                bool ok = true;
+                for (int u = 0; u < d.nunits && ok; ++u) {
+                    const bool fresh = fp8 || u == 0;
+                    if (fresh && !mbar_wait(&dempty[ds], dph ^ 1, abort_flag, err)) ok = false;
+                    if (ok && !mbar_wait(&afull[as], aph, abort_flag, err)) ok = false;
+                    if (ok && !mbar_wait(&bfull[bs], bph, abort_flag, err)) ok = false;
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t a0 = tmem + as * 128, a1 = a0 + 64;
+                    const uint32_t d0 = tmem + kDCol + ds * 64, d1 = d0 + 32;
+                    const uint32_t bb = smem_u32(bbuf + bs * kBStageBytes);
+#pragma unroll 1
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const bool acc = !(fresh && ks == 0);
+                        const uint64_t bh = smem_desc_noswz(bb + ks * 256, 128, 2048);
+                        mma_f16_ats(d0, a0 + ks * 8, bh, idesc, acc);
+                        mma_f16_ats(d1, a1 + ks * 8, bh, idesc, acc);
+                        if (d.kind == 1) {
+                            const uint64_t bl = smem_desc_noswz(bb + d.npad * 256 + ks * 256, 128, 2048);
+                            mma_f16_ats(d0, a0 + ks * 8, bl, idesc, true);
+                            mma_f16_ats(d1, a1 + ks * 8, bl, idesc, true);
+                        }
+                    }
+                    issued = true;
+                    mma_commit(&aempty[as]);
+                    mma_commit(&bempty[bs]);
+                    if (fp8 || u == d.nunits - 1) {
+                        mma_commit(&dfull[ds]);
+                        if (++ds == 2) {
+                            ds = 0;
+                            dph ^= 1;
+                        }
+                    }
+                    if (++as == kASlots) {
+                        as = 0;
+                        aph ^= 1;
+                    }
+                    if (++bs == kBStages) {
+                        bs = 0;
+                        bph ^= 1;
+                    }
+                }
+                if (!ok) break;
+            }
+            if (issued) {  // all MMAs retired before TMEM is released
+                mma_commit(drain);
+                const unsigned long long t0 = globaltimer_ns();
+                while (!mbar_try_wait(drain, 0) && globaltimer_ns() - t0 < kWaitBudgetNs) {
+                }
+            }
+        }
+    } else if (warp < 4) {
+        // ===================== B stagers (warps 2-3) =====================
+        // Each warp decides alone (lane votes), so an aborted wait never
+        // leaves a warp waiting at a barrier for another.
+        const int st = tid - 64;
+        int js = 0, jph = 0, bs = 0, bph = 0;
+        for (;;) {
+            if (!__all_sync(0xffffffffu, mbar_wait(&jfull[js], jph, abort_flag, err))) break;
+            const TcJob d = job_at(js);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&jempty[js]);
+            if (++js == kJobSlots) {
+                js = 0;
+                jph ^= 1;
+            }
+            if (d.kind < 0) break;
+            bool ok = true;
+            if (d.kind == 1 && warp == 2) {
+                // the group's intermediate must be complete: every row tile, every quarter
+                int okl = 1;
+                if (lane == 0) {
+                    const uint32_t need = (uint32_t)(4 * (d.Ig / 128));
+                    const uint32_t *flag = p.group_ready + d.pair;
+                    if (ld_acquire_gpu(flag) < need) {
+                        const unsigned long long t0 = globaltimer_ns();
+                        while (ld_acquire_gpu(flag) < need) {
+                            if (*abort_flag) {
+                                okl = 0;
+                                break;
+                            }
+                            if (globaltimer_ns() - t0 > kWaitBudgetNs) {
+                                atomicOr(err, kErrWaitTimeout);
+                                *abort_flag = 1;
+                                okl = 0;
+                                break;
+                            }
+                            __nanosleep(128);
+                        }
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, okl, 0) != 0;
+            }
+            for (int u = 0; u < d.nunits && ok; ++u) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&bempty[bs], bph ^ 1, abort_flag, err))) {
+                    ok = false;
+                    break;
+                }
+                uint8_t *dst = bbuf + bs * kBStageBytes;
+                const int ku = d.k0 / kUnitK + u;  // global K unit index
+                if (d.kind == 1) {
+                    if (lane == 0) {
+                        if (warp == 2) {
+                            // generic-proxy writes by other CTAs (acquired above) before
+                            // this async-proxy read
+                            asm volatile("fence.proxy.async.global;" ::: "memory");
+                            const uint32_t bytes = (uint32_t)d.npad * 512u;
+                            mbar_arrive_expect_tx(&bfull[bs], bytes);
+                            bulk_load(dst, p.midB + d.mid_off + (long long)ku * d.npad * 512, bytes, &bfull[bs]);
+                        } else {
+                            mbar_arrive(&bfull[bs]);
+                        }
+                    }
+                } else {
+                    // gather x columns, bf16 -> f16, core-matrix layout
+                    uint32_t range_bad = 0;
+                    for (int it = st; it < d.npad * 16; it += 64) {
+                        const int c = it >> 4, k8 = it & 15;
+                        uint4 v = make_uint4(0, 0, 0, 0);
+                        if (c < d.n) {
+                            const int t = crow[d.col0 + c];
+                            const uint4 q = __ldg(reinterpret_cast<const uint4 *>(
+                                p.x + (size_t)t * H + ku * kUnitK + k8 * 8));
+                            const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+                            uint32_t o[4];
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                const __half2 h = __floats2half2_rn(bf16_bits_to_float(w4[k] & 0xffffu),
+                                                                    bf16_bits_to_float(w4[k] >> 16));
+                                if (__hisinf(__low2half(h)) || __hisinf(__high2half(h))) range_bad = 1;
+                                o[k] = pack_h2(h);
+                            }
+                            v = make_uint4(o[0], o[1], o[2], o[3]);
+                        }
+                        *reinterpret_cast<uint4 *>(dst + b_off(c, k8 * 8)) = v;
+                    }
+                    if (range_bad) atomicOr(err, kErrRange);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bfull[bs]);
+                }
+                if (++bs == kBStages) {
+                    bs = 0;
+                    bph ^= 1;
+                }
+            }
+            if (!ok) break;
+        }
+    } else if (warp < 12) {
+        // ===================== dequant (tile0: warps 4-7, tile1: 8-11) =====================
+        const int wg = (warp - 4) >> 2;
+        const int r = ((warp & 3) << 5) | lane;  // row of the tile == TMEM lane
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        int js = 0, jph = 0, rs = 0, rph = 0, as = 0, aph = 0;
+        for (;;) {
+            if (!__all_sync(0xffffffffu, mbar_wait(&jfull[js], jph, abort_flag, err))) break;
+            const TcJob d = job_at(js);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&jempty[js]);
+            if (++js == kJobSlots) {
+                js = 0;
+                jph ^= 1;
+            }
+            if (d.kind < 0) break;
+            const bool fp4 = d.fmt == kFmtNvfp4;
+            const int upst = fp4 ? 2 : 1;
+            const int nst = d.nunits / upst;
+            bool ok = true;
+            for (int s = 0; s < nst && ok; ++s) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&rfull[rs], rph, abort_flag, err))) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t *tile = raw + rs * kRawStageBytes + wg * kRawTileBytes;
+                const uint8_t *row = tile + r * 128;
+                const int sw = r & 7;
+                for (int uu = 0; uu < upst; ++uu) {
+                    if (!__all_sync(0xffffffffu, mbar_wait(&aempty[as], aph ^ 1, abort_flag, err))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t tcol = tmem + lane_base + as * 128 + wg * 64;
+                    if (fp4) {
+                        const uint2 sc = *reinterpret_cast<const uint2 *>(
+                            raw + rs * kRawStageBytes + kRawScaleOff + wg * 2048 + r * 16 + uu * 8);
+                        const uint32_t scw[2] = {sc.x, sc.y};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const int chunk = uu * 4 + q;  // 16 B = 32 codes = 2 scale blocks
+                            const uint4 v = *reinterpret_cast<const uint4 *>(row + ((chunk ^ sw) << 4));
+                            const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+                            const __half2 s2 = e4m3x2_to_half2((scw[q >> 1] >> (16 * (q & 1))) & 0xffffu);
+                            const __half2 slo = __low2half2(s2), shi = __high2half2(s2);
+                            uint32_t o[16];
+#pragma unroll
+                            for (int b = 0; b < 16; ++b) {
+                                const __half2 h = e2m1x2_to_half2((vw[b >> 2] >> (8 * (b & 3))) & 0xffu);
+                                o[b] = pack_h2(__hmul2(h, b < 8 ? slo : shi));
+                            }
+                            tmem_st16(tcol + q * 16, o);
+                        }
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            uint32_t o[16];
+#pragma unroll
+                            for (int hq = 0; hq < 2; ++hq) {
+                                const int chunk = q * 2 + hq;
+                                const uint4 v = *reinterpret_cast<const uint4 *>(row + ((chunk ^ sw) << 4));
+                                const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                                for (int b = 0; b < 8; ++b)
+                                    o[hq * 8 + b] = pack_h2(e4m3x2_to_half2((vw[b >> 1] >> (16 * (b & 1))) & 0xffffu));
+                            }
+                            tmem_st16(tcol + q * 16, o);
+                        }
+                    }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&afull[as]);
+                    if (++as == kASlots) {
+                        as = 0;
+                        aph ^= 1;
+                    }
+                }
+                if (!ok) break;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&rempty[rs]);
+                if (++rs == kRawStages) {
+                    rs = 0;
+                    rph ^= 1;
+                }
+            }
+            if (!ok) break;
+        }
+    } else {
+        // ===================== epilogue (warps 12-15) =====================
+        // Each warp owns 32 rows of the tile (its TMEM lane quarter) and runs
+        // the reductions for those rows on its own: counters are kept per
+        // (tile, quarter), so no warp ever waits for another.
+        const int quarter = warp & 3;
+        const int r = (quarter << 5) | lane;
+        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        int js = 0, jph = 0, ds = 0, dph = 0;
+        for (;;) {
+            if (!__all_sync(0xffffffffu, mbar_wait(&jfull[js], jph, abort_flag, err))) break;
+            const TcJob d = job_at(js);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&jempty[js]);
+            if (++js == kJobSlots) {
+                js = 0;
+                jph ^= 1;
+            }
+            if (d.kind < 0) break;
+            const bool fp8 = d.fmt == kFmtFp8B128;
+            const WeightsDev &W = d.shared ? p.shared : p.routed;
+            float acc0[kNt], acc1[kNt];
+#pragma unroll
+            for (int c = 0; c < kNt; ++c) acc0[c] = acc1[c] = 0.0f;
+            const int nacc = fp8 ? d.nunits : 1;
+            bool ok = true;
+            for (int a = 0; a < nacc; ++a) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&dfull[ds], dph, abort_flag, err))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t dcol = tmem + lane_base + kDCol + ds * 64;
+                float s0 = 1.0f, s1 = 1.0f;
+                if (fp8) {
+                    const int ku = d.k0 / kUnitK + a;  // 128-K block index along the input dim
+                    const float *sc = reinterpret_cast<const float *>(d.kind == 0 ? W.w13_scale : W.w2_scale);
+                    const int rows = d.kind == 0 ? 2 * d.Ig : H;
+                    const int cols_blk = (d.kind == 0 ? H : d.Ig) / 128;
+                    const size_t base = (size_t)d.e * (rows / 128);
+                    s0 = __ldg(sc + (base + d.rows0 / 128) * cols_blk + ku);
+                    s1 = (d.rows1 < rows) ? __ldg(sc + (base + d.rows1 / 128) * cols_blk + ku) : 0.0f;
+                }
+#pragma unroll
+                for (int cb = 0; cb < kNt; cb += 16) {
+                    if (cb < d.npad) {
+                        uint32_t v0[16], v1[16];
+                        tmem_ld16(dcol + cb, v0);
+                        tmem_ld16(dcol + 32 + cb, v1);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            if (fp8) {
+                                acc0[cb + j] = __fmaf_rn(s0, __uint_as_float(v0[j]), acc0[cb + j]);
+                                acc1[cb + j] = __fmaf_rn(s1, __uint_as_float(v1[j]), acc1[cb + j]);
+                            } else {
+                                acc0[cb + j] = __uint_as_float(v0[j]);
+                                acc1[cb + j] = __uint_as_float(v1[j]);
+                            }
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&dempty[ds]);
+                if (++ds == 2) {
+                    ds = 0;
+                    dph ^= 1;
+                }
+            }
+            if (!ok) break;
+
+            if (d.kind == 0) {
+                // ---- gate/up: partial sums, the last chunk reduces, SwiGLU ----
+                const int i = d.tile * 128 + r;  // intermediate row
+                bool last = true;
+                if (d.nkc > 1) {
+#pragma unroll
+                    for (int c = 0; c < kNt; ++c)
+                        if (c < d.n) {
+                            const size_t col = (size_t)(d.col0 + c);
+                            p.P[(((size_t)d.kc * 2 + 0) * p.Ucap + col) * p.Imax + i] = acc0[c];
+                            p.P[(((size_t)d.kc * 2 + 1) * p.Ucap + col) * p.Imax + i] = acc1[c];
+                        }
+                    __threadfence();
+                    __syncwarp();
+                    int l = 0;
+                    if (lane == 0)
+                        l = atom_add_acq_rel_gpu(p.tile_cnt + (size_t)d.tile_id * 4 + quarter, 1u) ==
+                            (uint32_t)d.nkc - 1;
+                    last = __shfl_sync(0xffffffffu, l, 0) != 0;
+                    if (last) {
+                        __threadfence();
+#pragma unroll
+                        for (int c = 0; c < kNt; ++c)
+                            if (c < d.n) {
+                                const size_t col = (size_t)(d.col0 + c);
+                                float sg = __ldcg(p.P + ((size_t)0 * p.Ucap + col) * p.Imax + i);
+                                float su = __ldcg(p.P + ((size_t)1 * p.Ucap + col) * p.Imax + i);
+                                for (int kc = 1; kc < d.nkc; ++kc) {
+                                    sg = __fadd_rn(sg, __ldcg(p.P + (((size_t)kc * 2 + 0) * p.Ucap + col) * p.Imax + i));
+                                    su = __fadd_rn(su, __ldcg(p.P + (((size_t)kc * 2 + 1) * p.Ucap + col) * p.Imax + i));
+                                }
+                                acc0[c] = sg;
+                                acc1[c] = su;
+                            }
+                        if (lane == 0) p.tile_cnt[(size_t)d.tile_id * 4 + quarter] = 0;
+                    }
+                }
+                if (last) {
+                    const float gs = (d.fmt == kFmtNvfp4) ? __ldg(W.w13_gscale + d.e) : 1.0f;
+                    uint8_t *mb = p.midB + d.mid_off + (long long)d.tile * d.npad * 512;
+                    uint32_t range_bad = 0;
+#pragma unroll
+                    for (int c = 0; c < kNt; ++c)
+                        if (c < d.npad) {
+                            __half hi = __float2half_rn(0.0f), lo = hi;
+                            if (c < d.n) {
+                                const float g = (d.fmt == kFmtNvfp4) ? __fmul_rn(acc0[c], gs) : acc0[c];
+                                const float u = (d.fmt == kFmtNvfp4) ? __fmul_rn(acc1[c], gs) : acc1[c];
+                                const float m = __fmul_rn(silu_f32(g), u);
+                                hi = __float2half_rn(m);
+                                lo = __float2half_rn(__fsub_rn(m, __half2float(hi)));
+                                if (__hisinf(hi) || !(fabsf(m) == fabsf(m))) range_bad = 1;
+                            }
+                            *reinterpret_cast<__half *>(mb + b_off(c, r)) = hi;
+                            *reinterpret_cast<__half *>(mb + d.npad * 256 + b_off(c, r)) = lo;
+                        }
+                    if (range_bad) atomicOr(err, kErrRange);
+                    __threadfence();
+                    __syncwarp();
+                    if (lane == 0) atom_add_acq_rel_gpu(p.group_ready + d.pair, 1u);
+                }
+            } else {
+                // ---- down: per-chunk outputs; the last job on a 256-row tile combines ----
+                const int h0 = d.rows0 + r, h1 = d.rows1 + r;
+#pragma unroll
+                for (int c = 0; c < kNt; ++c)
+                    if (c < d.n) {
+                        const size_t col = (size_t)(d.col0 + c);
+                        float *y = p.Y + ((size_t)d.kc * p.Ucap + col) * H;
+                        if (h0 < H) y[h0] = acc0[c];
+                        if (h1 < H) y[h1] = acc1[c];
+                    }
+                __threadfence();
+                __syncwarp();
+                int l = 0;
+                if (lane == 0)
+                    l = atom_add_acq_rel_gpu(p.htile_cnt + (size_t)d.tile * 4 + quarter, 1u) ==
+                        (uint32_t)dn_per_ht - 1;
+                const bool last = __shfl_sync(0xffffffffu, l, 0) != 0;
+                if (last) {
+                    __threadfence();
+                    const int nkc_s = tc_nkc_dn(p.Is, T), nkc_r = tc_nkc_dn(p.I, T);
+                    const float gs_s = p.shared.fmt == kFmtNvfp4 ? __ldg(p.shared.w2_gscale) : 1.0f;
+                    for (int t = 0; t < T; ++t) {
+                        const int32_t *rc = rcol + t * (K + 1);
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const int h = hh ? h1 : h0;
+                            if (h >= H) continue;
+                            float acc = __bfloat162float(p.x[(size_t)t * H + h]);
+                            {
+                                const size_t col = (size_t)rc[0];
+                                float y = __ldcg(p.Y + col * H + h);
+                                for (int kc = 1; kc < nkc_s; ++kc)
+                                    y = __fadd_rn(y, __ldcg(p.Y + ((size_t)kc * p.Ucap + col) * H + h));
+                                acc = __fadd_rn(acc, __fmul_rn(y, gs_s));
+                            }
+                            for (int q = 0; q < K; ++q) {
+                                const int c = rc[1 + q];
+                                if (c < 0) continue;
+                                float y = __ldcg(p.Y + (size_t)c * H + h);
+                                for (int kc = 1; kc < nkc_r; ++kc)
+                                    y = __fadd_rn(y, __ldcg(p.Y + ((size_t)kc * p.Ucap + c) * H + h));
+                                const float gs = p.routed.fmt == kFmtNvfp4
+                                                     ? __ldg(p.routed.w2_gscale + p.ids[t * K + q])
+                                                     : 1.0f;
+                                acc = __fmaf_rn(p.topk_w[t * K + q], __fmul_rn(y, gs), acc);
+                            }
+                            p.out[(size_t)t * H + h] = __float2bfloat16_rn(acc);
+                        }
+                    }
+                    if (lane == 0) p.htile_cnt[(size_t)d.tile * 4 + quarter] = 0;
+                }
+            }
+        }
+    }
+
+    // ---- teardown -----------------------------------------------------------
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+    if (tid == 0) {
+        __threadfence();
+        if (atom_add_acq_rel_gpu(&p.hdr->exit_cnt, 1u) == gridDim.x - 1) {
+            // every CTA is done with the counters: leave them zero for the next launch
+            for (int i = 0; i < pair_prefix[G]; ++i) p.group_ready[i] = 0;
+            p.hdr->job_next = 0;
+            __threadfence();
+            p.hdr->exit_cnt = 0;
+            __threadfence();
+        }
+    }
+}
+
+}  // namespace moe

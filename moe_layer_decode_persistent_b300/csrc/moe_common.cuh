@@ -43,7 +43,9 @@ struct WsHeader {
     uint32_t err;        // device error word (MOE_DEV_* bits)
     uint32_t bar_count;  // grid barrier: arrivals in the current round
     uint32_t bar_gen;    // grid barrier: completed rounds (monotonic)
-    uint32_t pad[61];
+    uint32_t job_next;   // tensor-core path: next job to claim
+    uint32_t exit_cnt;   // tensor-core path: CTAs finished
+    uint32_t pad[59];
 };
 static_assert(sizeof(WsHeader) == 256, "header size");
 

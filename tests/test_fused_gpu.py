@@ -13,15 +13,15 @@ from gpu_util import (assert_parity, layer, oracle_ref, run_fused, shape_of, wor
 
 pytestmark = pytest.mark.gpu
 
-PATHS = {"fma": B.MOE_FLAG_FORCE_FMA, "auto": 0}
+PATHS = {"fma": B.MOE_FLAG_FORCE_FMA, "mma": B.MOE_FLAG_FORCE_MMA, "auto": 0}
 
-SMALL = inputs.Shape(T=5, H=512, I=256, I_shared=384, E=16, K=4)
+SMALL = inputs.Shape(T=5, H=512, I=256, I_shared=512, E=16, K=4)
 FORMATS = {"nvfp4/fp8": (inputs.FMT_NVFP4, inputs.FMT_FP8_B128),
            "fp8/nvfp4": (inputs.FMT_FP8_B128, inputs.FMT_NVFP4),
            "bf16/bf16": (inputs.FMT_BF16, inputs.FMT_BF16)}
 
 
-@pytest.mark.parametrize("path", list(PATHS))
+@pytest.mark.parametrize("path", ["fma", "auto"])
 def test_tiny_bf16_layer(path):
     L = inputs.make_tiny(0, "cuda")
     out = run_fused(L, PATHS[path])
@@ -32,6 +32,8 @@ def test_tiny_bf16_layer(path):
 @pytest.mark.parametrize("fmt", list(FORMATS))
 @pytest.mark.parametrize("T", [1, 3, 5, 13])
 def test_small_layers_all_formats(path, fmt, T):
+    if path == "mma" and fmt == "bf16/bf16":
+        pytest.skip("bf16 weights run on the CUDA-core path")
     s = inputs.Shape(T=T, H=SMALL.H, I=SMALL.I, I_shared=SMALL.I_shared, E=SMALL.E, K=SMALL.K)
     L = layer(s, "zipf", seed=T, fr=FORMATS[fmt][0], fs=FORMATS[fmt][1], used_only=False)
     out = run_fused(L, PATHS[path])
@@ -40,7 +42,7 @@ def test_small_layers_all_formats(path, fmt, T):
 
 @pytest.mark.parametrize("path", list(PATHS))
 def test_non_power_of_two_k(path):
-    s = inputs.Shape(T=7, H=256, I=128, I_shared=256, E=12, K=6)
+    s = inputs.Shape(T=7, H=256, I=256, I_shared=512, E=12, K=6)
     L = layer(s, "mtp", seed=1, used_only=False)
     assert_parity(run_fused(L, PATHS[path]), oracle_ref(L))
 
@@ -70,7 +72,7 @@ def test_dsv3_t64_zipf_sampled_rows(path):
 @pytest.mark.parametrize("case", ["small_zipf_T13", "dsv3_T8_mtp", "dsv3_T64_zipf"])
 def test_dedup_is_bitwise_equal_to_one_row_form(path, case):
     if case == "small_zipf_T13":
-        s = inputs.Shape(T=13, H=512, I=256, I_shared=384, E=16, K=4)
+        s = inputs.Shape(T=13, H=512, I=256, I_shared=512, E=16, K=4)
         L = layer(s, "zipf", seed=2, used_only=False)
     elif case == "dsv3_T8_mtp":
         L = layer(inputs.dsv3(8), "mtp", seed=1)
@@ -93,7 +95,7 @@ def test_repeat_launches_are_identical(path):
 
 @pytest.mark.parametrize("path", list(PATHS))
 def test_duplicate_rows_and_permutation(path):
-    s = inputs.Shape(T=9, H=512, I=256, I_shared=384, E=16, K=4)
+    s = inputs.Shape(T=9, H=512, I=256, I_shared=512, E=16, K=4)
     L = layer(s, "uniform", seed=4, used_only=False)
     L.x[5] = L.x[2]
     L.topk_ids[5] = L.topk_ids[2]
@@ -110,7 +112,7 @@ def test_duplicate_rows_and_permutation(path):
 @pytest.mark.parametrize("path", list(PATHS))
 def test_negative_controls(path):
     """Each perturbation changes exactly the outputs that depend on it."""
-    s = inputs.Shape(T=6, H=512, I=256, I_shared=384, E=16, K=4)
+    s = inputs.Shape(T=6, H=512, I=256, I_shared=512, E=16, K=4)
     L = layer(s, "uniform", seed=5, used_only=False)
     base = run_fused(L, PATHS[path]).view(torch.int16).clone()
 
@@ -138,7 +140,7 @@ def test_negative_controls(path):
 
 @pytest.mark.parametrize("path", list(PATHS))
 def test_zero_down_weights_give_residual(path):
-    s = inputs.Shape(T=4, H=256, I=128, I_shared=128, E=8, K=2)
+    s = inputs.Shape(T=4, H=256, I=256, I_shared=256, E=8, K=2)
     L = layer(s, "uniform", seed=6, used_only=False)
     L.routed.w2.zero_()
     L.shared.w2.zero_()
