@@ -37,6 +37,8 @@ WORKLOADS = {
 N_COPIES = 4
 KERNEL_SOURCES = ["moe_layer_decode_persistent_b300/csrc/api.cu",
                   "moe_layer_decode_persistent_b300/csrc/fused_fma.cuh",
+                  "moe_layer_decode_persistent_b300/csrc/fused_tc.cuh",
+                  "moe_layer_decode_persistent_b300/csrc/sm100.cuh",
                   "moe_layer_decode_persistent_b300/csrc/group_table.cuh",
                   "moe_layer_decode_persistent_b300/csrc/moe_common.cuh"]
 
@@ -172,10 +174,10 @@ def run_ours(args, rank, world, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     wl = WORKLOADS[args.workload]
-    shape = inputs.dsv3(wl["T"])
+    shape = inputs.dsv3(wl["T"], E=args.experts)
     L = inputs.make_layer(shape, wl["routing"], 0, dev, inputs.FMT_NVFP4, inputs.FMT_FP8_B128)
     copies = [(L.routed, L.shared)]
-    for _ in range(N_COPIES - 1):
+    for _ in range(args.copies - 1):
         r = inputs.ExpertSet(**{k: (v.clone() if isinstance(v, torch.Tensor) else v)
                                 for k, v in L.routed.__dict__.items()})
         s = inputs.ExpertSet(**{k: (v.clone() if isinstance(v, torch.Tensor) else v)
@@ -190,7 +192,7 @@ def run_ours(args, rank, world, local):
     algo_bytes, distinct = algorithmic_bytes(L, L.topk_ids.cpu())
 
     def launch(i):
-        rw, sw = weights[i % N_COPIES]
+        rw, sw = weights[i % len(weights)]
         B.moe_fused_decode(L.x, L.topk_ids, L.topk_w, rw, sw, out, sh, ws, stream=stream)
 
     for i in range(args.warmup):
@@ -221,13 +223,17 @@ def run_ours(args, rank, world, local):
     us_launch_max = max_over_ranks(us_launch, world, dev)
 
     # end to end through the host-buffer entry point (pinned buffers, copies inside)
+    if args.no_e2e:
+        return dict(us_launch=us_launch_max, ms_per_step=ms_per_step, algo_bytes=algo_bytes,
+                    distinct=distinct, clocks=clk.summary(), err=err, e2e_us=None, h2d=0, d2h=0,
+                    sweep={}, T=shape.T)
     xh = L.x.cpu().pin_memory()
     ih = L.topk_ids.cpu().pin_memory()
     wh = L.topk_w.cpu().pin_memory()
     oh = torch.empty_like(xh).pin_memory()
 
     def launch_host(i):
-        rw, sw = weights[i % N_COPIES]
+        rw, sw = weights[i % len(weights)]
         B.moe_fused_decode_host(xh, ih, wh, rw, sw, oh, sh, ws, stream=stream)
 
     for i in range(max(3, args.warmup)):
@@ -354,14 +360,19 @@ def main():
     ap.add_argument("--flags", type=int, default=0)
     ap.add_argument("--sweep", action="store_true", help="also time the T=8 and T=64 workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer (end-to-end) timing")
+    ap.add_argument("--experts", type=int, default=256,
+                    help="routed experts E (profiling runs use fewer to bound device memory)")
+    ap.add_argument("--copies", type=int, default=N_COPIES,
+                    help="resident weight copies rotated per step")
     args = ap.parse_args()
     rank, world, local = dist_setup(args)
     T = WORKLOADS[args.workload]["T"]
     metric = "us per MoE-layer launch"
     config = {"workload": f"{args.workload}: DeepSeek-V3-shaped decode MoE layer, T={T}, H=7168, "
-                          f"routed I=2048 NVFP4 E=256 top-8, shared I=2048 FP8 128x128, "
+                          f"routed I=2048 NVFP4 E={args.experts} top-8, shared I=2048 FP8 128x128, "
                           f"{WORKLOADS[args.workload]['routing']} routing",
-              "T": T, "l2": f"{N_COPIES} resident weight copies rotated per step (inputs larger than L2)"}
+              "T": T, "l2": f"{args.copies} resident weight copies rotated per step (inputs larger than L2)"}
 
     if args.impl == "reference":
         if rank != 0:
@@ -386,7 +397,8 @@ def main():
         return
     peak, peak_kind = measured_peaks()
     gbs = r["algo_bytes"] / (r["us_launch"] * 1e-6) / 1e9
-    trec = traffic_record("fused_fma_kernel")
+    kname = "fused_fma_kernel" if (args.flags & 2) else "fused_tc_kernel"
+    trec = traffic_record(kname)
     line = {
         "metric": metric, "value": round(r["us_launch"], 2), "unit": "us", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(r["ms_per_step"], 4),
@@ -397,9 +409,10 @@ def main():
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(gbs / peak, 4), "peak_kind": peak_kind,
                      "traffic": (trec or {}).get("dram_bytes_per_launch"),
-                     "kernel": "fused_fma_kernel"},
-        "e2e": {"value": round(r["e2e_us"], 2), "unit": "us", "h2d_bytes_per_step": r["h2d"],
-                "d2h_bytes_per_step": r["d2h"]},
+                     "kernel": kname},
+        "e2e": None if r["e2e_us"] is None else
+        {"value": round(r["e2e_us"], 2), "unit": "us", "h2d_bytes_per_step": r["h2d"],
+         "d2h_bytes_per_step": r["d2h"]},
         "gpu_launches": args.steps, "clocks": r["clocks"], "device_error_word": r["err"],
     }
     if r["sweep"]:

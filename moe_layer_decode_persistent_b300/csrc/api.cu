@@ -38,13 +38,13 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Workspace. Both kernels share the 256-byte header (error word, counters).
 //   CUDA-core path : header | mid fp32 [Ucap][Imax] | y fp32 [Ucap][H]
-//   tensor path    : header | group_ready [C] | tile_cnt [C*Imax/128*4] |
-//                    htile_cnt [H/256*4] | P | Y | midB
+//   tensor path    : header | group_ready [C] | x_ready [C] |
+//                    tile_cnt [C*Imax/128*4] | htile_cnt [H/256*4] | P | Y | midB | xB
 // followed by the host-buffer call's staging area. Ucap = C = T*(K+1).
 struct WsLayout {
     size_t mid = 0, y = 0, fma_end = 0;
-    size_t tc_ready = 0, tc_tile = 0, tc_htile = 0, tc_ctrl_end = 0, tc_P = 0, tc_Y = 0, tc_midB = 0,
-           tc_end = 0;
+    size_t tc_ready = 0, tc_xready = 0, tc_tile = 0, tc_htile = 0, tc_ctrl_end = 0, tc_P = 0, tc_Y = 0,
+           tc_midB = 0, tc_xB = 0, tc_end = 0;
     size_t dev_total = 0;
     size_t st_x = 0, st_ids = 0, st_w = 0, st_out = 0, host_total = 0;
 };
@@ -65,6 +65,8 @@ WsLayout ws_layout(const moe_shape *s) {
     off = sizeof(moe::WsHeader);
     L.tc_ready = off;
     off += Ucap * 4;
+    L.tc_xready = off = align_up(off, 16);
+    off += Ucap * 4;
     L.tc_tile = off = align_up(off, 16);
     off += Ucap * (Imax / 128) * 4 * 4;
     L.tc_htile = off = align_up(off, 16);
@@ -80,7 +82,9 @@ WsLayout ws_layout(const moe_shape *s) {
     L.tc_Y = off = align_up(off, 256);
     off += (size_t)moe::tc_nkc_dn((int)Imax, Ti) * Ucap * H * sizeof(float);
     L.tc_midB = off = align_up(off, 256);
-    off += 16 * Ucap * (Imax / 128) * 512;  // sum of padded column counts <= 16 * Ucap
+    off += 16 * Ucap * (Imax / 128) * 256;  // sum of padded column counts <= 16 * Ucap
+    L.tc_xB = off = align_up(off, 256);
+    off += 16 * Ucap * H * 2;
     L.tc_end = align_up(off, 256);
 
     L.dev_total = off = std::max(L.fma_end, L.tc_end);
@@ -392,6 +396,8 @@ moe_status launch_fused_tc(const moe::FusedParams &fp, const WsLayout &L, const 
     p.P = reinterpret_cast<float *>(ws + L.tc_P);
     p.Y = reinterpret_cast<float *>(ws + L.tc_Y);
     p.midB = reinterpret_cast<uint8_t *>(ws + L.tc_midB);
+    p.xB = reinterpret_cast<uint8_t *>(ws + L.tc_xB);
+    p.x_ready = reinterpret_cast<uint32_t *>(ws + L.tc_xready);
     p.Ucap = s->T * (s->K + 1);
     p.Imax = std::max(s->I, s->I_shared);
     const size_t smem = (size_t)moe::tc_smem_bytes(s->T, s->K);

@@ -17,27 +17,32 @@
 //     tile0 = rows ht*256.., tile1 = rows ht*256+128.., K = I chunk
 // Both tiles of a job share the B operand (the group's activation columns).
 //
-// Per CTA the roles are warp-specialised (16 warps):
+// Per CTA the roles are warp-specialised (18 warps):
 //   warp 0      producer: claims jobs, TMA-loads 128-byte-wide weight boxes
 //               (SWIZZLE_128B) and NVFP4 block scales into a 3-stage ring
-//   warp 1      MMA issuer: tcgen05.mma kind::f16, M=128, N=16|32, K=16,
-//               A from TMEM, B from shared memory; commits to mbarriers
-//   warps 2-3   B stagers: gather + convert activation columns bf16->f16
-//               (gate/up) or bulk-copy the split f16 intermediate (down)
-//   warps 4-7   dequant of tile0, warps 8-11 dequant of tile1: one thread per
+//   warp 1      B stager: bulk-copies the job's B tile per 128-K unit, the
+//               f16 activation columns (gate/up; converted once per launch in
+//               the prologue, spread over all CTAs) or the f16 intermediate
+//               (down), after waiting for its producers
+//   warps 2-5   MMA issuers: tcgen05.mma kind::f16, M=128, N=16|32, K=16,
+//               A from TMEM, B from shared memory. One issuing thread sustains
+//               one MMA per ~120 cycles whatever N is, so four issuers split
+//               each unit: issuer q takes tile q&1, K-steps of half q>>1, into
+//               its own accumulator (the halves are added in a fixed order)
+//   warps 6-9   dequant of tile0, warps 10-13 dequant of tile1: one thread per
 //               weight row, E2M1*E4M3 -> exact f16 (or E4M3 -> f16), written
 //               to TMEM as the MMA's A operand (the weights never touch
 //               shared memory as f16)
-//   warps 12-15 epilogue: TMEM accumulators -> registers; FP8 128x128 block
+//   warps 14-17 epilogue: TMEM accumulators -> registers; FP8 128x128 block
 //               scales applied per 128-K block in fp32; partial sums, the
-//               fixed-order reductions, SwiGLU, the split f16 intermediate,
-//               and the final combine + single bf16 write
+//               fixed-order reductions, SwiGLU, the f16 intermediate, and the
+//               final combine + single bf16 write
 //
 // Precision: weights dequantise exactly to f16 (e2m1*e4m3 has <= 6
 // significant bits); activations bf16 -> f16 (exact for |x| in [2^-17, 65504];
-// larger magnitudes set MOE_DEV_RANGE); the fp32 SwiGLU intermediate is split
-// hi = f16(m), lo = f16(m - hi) and both halves go through the MMA; every
-// accumulation is fp32.
+// larger magnitudes set MOE_DEV_RANGE); the fp32 SwiGLU intermediate is
+// rounded once to f16 for the down MMA (relative error <= 2^-12 per element,
+// about 1.4e-4 |y| rms on the down output); every accumulation is fp32.
 #pragma once
 
 #include <cuda.h>
@@ -48,20 +53,23 @@
 
 namespace moe {
 
-constexpr int kTcThreads = 512;
+constexpr int kTcThreads = 576;
 constexpr int kTcMaxT = 64;
-constexpr int kNt = 32;               // columns per job at most
+constexpr int kNt = 32;               // columns per job at most (NVFP4)
+constexpr int kNtFp8 = 16;            // FP8 jobs: fp32 block-scale promotion in registers
 constexpr int kUnitK = 128;           // K elements of one TMEM A unit per tile
-constexpr int kRawStages = 3;
+constexpr int kRawStages = 4;
 constexpr int kRawTileBytes = 16384;  // 128 rows x 128 bytes
 constexpr int kRawScaleOff = 2 * kRawTileBytes;
 constexpr int kRawStageBytes = 2 * kRawTileBytes + 2 * 2048;  // + NVFP4 scales
-constexpr int kBStages = 3;
-constexpr int kBStageBytes = 2 * kNt * kUnitK * 2;  // hi + lo f16
-constexpr int kASlots = 3;
+constexpr int kBStages = 4;
+constexpr int kBStageBytes = kNt * kUnitK * 2;  // f16 [32][128]
+constexpr int kASlots = 2;
+constexpr int kIssuers = 4;
 constexpr int kJobSlots = 4;
 constexpr int kTmemCols = 512;
-constexpr int kDCol = kASlots * 128;  // two D sets of (32 + 32) columns follow
+constexpr int kDCol = kASlots * 128;  // two D sets of 4 x 32 columns follow
+__host__ __device__ constexpr int tc_nt(int fmt) { return fmt == kFmtFp8B128 ? kNtFp8 : kNt; }
 constexpr int kKcNvfp4 = 1792;
 constexpr int kKcFp8 = 1024;
 constexpr int kKcDown = 1024;
@@ -86,7 +94,9 @@ struct TcParams {
     uint32_t *htile_cnt;    // per 256-row output tile
     float *P;               // gate/up partials [kc][2][Ucap][Imax]
     float *Y;               // down partials [kc][Ucap][H]
-    uint8_t *midB;          // split intermediate in MMA B layout
+    uint8_t *midB;          // f16 intermediate in MMA B layout
+    uint8_t *xB;            // activation columns, f16, MMA B layout per (group, column tile)
+    uint32_t *x_ready;      // per (group, column tile): columns converted
     int Ucap, Imax;
 };
 
@@ -99,6 +109,7 @@ struct TcJob {
     int rows0, rows1;
     int tile_id, pair;
     long long mid_off;  // bytes into midB of this (group, column tile)
+    long long x_off;    // bytes into xB of this (group, column tile)
 };
 
 // ---- per-launch constants shared by host and device -----------------------
@@ -124,15 +135,16 @@ __device__ __forceinline__ uint32_t b_off(int n, int k) {
 // Shared-memory layout of the fused kernel (dynamic, 1024-aligned base).
 struct TcSmem {
     static constexpr int raw = 0;
-    static constexpr int bbuf = raw + kRawStages * kRawStageBytes;  // 110592
-    static constexpr int jobs = bbuf + kBStages * kBStageBytes;      // 159744
+    static constexpr int bbuf = raw + kRawStages * kRawStageBytes;
+    static constexpr int jobs = bbuf + kBStages * kBStageBytes;
     static constexpr int bars = jobs + kJobSlots * (int)sizeof(TcJob);
-    // mbarriers: jfull, jempty, rfull, rempty, afull, aempty, bfull, bempty, dfull, dempty, drain
-    static constexpr int nbars = 2 * kJobSlots + 2 * kRawStages + 2 * kASlots + 2 * kBStages + 2 * 2 + 1;
+    // jfull, jempty, rfull, rempty, afull, aempty, bfull, bempty, dfull, dempty, drain[4]
+    static constexpr int nbars =
+        2 * kJobSlots + 2 * kRawStages + 2 * kASlots + 2 * kBStages + 2 * 2 + kIssuers;
     static constexpr int misc = bars + nbars * 8;  // tmem addr, abort, flags
     static constexpr int tables = misc + 64;       // group table, then per-group arrays
 };
-constexpr int kTcGroupArrays = 6;  // gu_prefix, dn_prefix, tile_prefix, mid_prefix, pair_prefix (+1 spare)
+constexpr int kTcGroupArrays = 6;  // gu, dn, tile, mid, pair and x-column prefix sums
 
 __host__ __device__ inline int tc_smem_bytes(int T, int K) {
     const int C = T * (K + 1);
@@ -141,7 +153,16 @@ __host__ __device__ inline int tc_smem_bytes(int T, int K) {
 
 __device__ __forceinline__ uint32_t pack_h2(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
 
-__device__ __forceinline__ __half2 u32_h2(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
+// group of column c: the last g with g0[g] <= c
+__device__ __forceinline__ int group_of_col(const int32_t *g0, int G, int c) {
+    int lo = 0, hi = G - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (g0[mid] <= c) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
 
 __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_constant__ TcParams p) {
     using namespace sm100;
@@ -172,6 +193,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
     int *tile_prefix = dn_prefix + (C + 1);
     int *mid_prefix = tile_prefix + (C + 1);
     int *pair_prefix = mid_prefix + (C + 1);
+    int *xcol_prefix = pair_prefix + (C + 1);
     uint32_t *err = &p.hdr->err;
 
     // ---- prologue: group table (scratch aliases the raw ring), per-group sums
@@ -181,60 +203,58 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
     const int32_t *gexp = tab.gexp(), *gn = tab.gncols(), *g0 = tab.gcol0(), *rcol = tab.row_col();
     const int *crow = tab.col_row();
     if (warp == 0) {
-        int run_gu = 0, run_dn = 0, run_tile = 0, run_mid = 0, run_pair = 0;
+        int run[6] = {0, 0, 0, 0, 0, 0};
         for (int base = 0; base < G; base += 32) {
             const int g = base + lane;
-            int v_gu = 0, v_dn = 0, v_tile = 0, v_mid = 0, v_pair = 0;
+            int v[6] = {0, 0, 0, 0, 0, 0};  // gu jobs, dn jobs, tiles, mid units, pairs, x columns
             if (g < G) {
                 const bool sh = gexp[g] < 0;
                 const int fmt = sh ? p.shared.fmt : p.routed.fmt;
                 const int Ig = sh ? p.Is : p.I;
-                const int n = gn[g], nct = (n + kNt - 1) / kNt;
+                const int nt = tc_nt(fmt);
+                const int n = gn[g], nct = (n + nt - 1) / nt;
                 const int tiles = Ig / 128;
-                v_pair = nct;
-                v_tile = nct * tiles;
-                v_gu = v_tile * tc_nkc_gu(fmt, H, T);
-                v_dn = nct * (H / 256) * tc_nkc_dn(Ig, T);
                 int np = 0;
-                for (int ct = 0; ct < nct; ++ct) np += ((min(kNt, n - ct * kNt) + 15) / 16) * 16;
-                v_mid = np * tiles;
+                for (int ct = 0; ct < nct; ++ct) np += ((min(nt, n - ct * nt) + 15) / 16) * 16;
+                v[0] = nct * tiles * tc_nkc_gu(fmt, H, T);
+                v[1] = nct * (H / 256) * tc_nkc_dn(Ig, T);
+                v[2] = nct * tiles;
+                v[3] = np * tiles;
+                v[4] = nct;
+                v[5] = np;
             }
-            int s_gu = v_gu, s_dn = v_dn, s_tile = v_tile, s_mid = v_mid, s_pair = v_pair;
+            int sc[6];
+#pragma unroll
+            for (int a = 0; a < 6; ++a) sc[a] = v[a];
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
-                const int a = __shfl_up_sync(0xffffffffu, s_gu, o), b = __shfl_up_sync(0xffffffffu, s_dn, o),
-                          c = __shfl_up_sync(0xffffffffu, s_tile, o), d = __shfl_up_sync(0xffffffffu, s_mid, o),
-                          f = __shfl_up_sync(0xffffffffu, s_pair, o);
-                if (lane >= o) {
-                    s_gu += a;
-                    s_dn += b;
-                    s_tile += c;
-                    s_mid += d;
-                    s_pair += f;
+#pragma unroll
+                for (int a = 0; a < 6; ++a) {
+                    const int y = __shfl_up_sync(0xffffffffu, sc[a], o);
+                    if (lane >= o) sc[a] += y;
                 }
             }
             if (g < G) {
-                gu_prefix[g] = run_gu + s_gu - v_gu;
-                dn_prefix[g] = run_dn + s_dn - v_dn;
-                tile_prefix[g] = run_tile + s_tile - v_tile;
-                mid_prefix[g] = run_mid + s_mid - v_mid;
-                pair_prefix[g] = run_pair + s_pair - v_pair;
+                gu_prefix[g] = run[0] + sc[0] - v[0];
+                dn_prefix[g] = run[1] + sc[1] - v[1];
+                tile_prefix[g] = run[2] + sc[2] - v[2];
+                mid_prefix[g] = run[3] + sc[3] - v[3];
+                pair_prefix[g] = run[4] + sc[4] - v[4];
+                xcol_prefix[g] = run[5] + sc[5] - v[5];
             }
-            run_gu += __shfl_sync(0xffffffffu, s_gu, 31);
-            run_dn += __shfl_sync(0xffffffffu, s_dn, 31);
-            run_tile += __shfl_sync(0xffffffffu, s_tile, 31);
-            run_mid += __shfl_sync(0xffffffffu, s_mid, 31);
-            run_pair += __shfl_sync(0xffffffffu, s_pair, 31);
+#pragma unroll
+            for (int a = 0; a < 6; ++a) run[a] += __shfl_sync(0xffffffffu, sc[a], 31);
         }
         if (lane == 0) {
-            gu_prefix[G] = run_gu;
-            dn_prefix[G] = run_dn;
-            tile_prefix[G] = run_tile;
-            mid_prefix[G] = run_mid;
-            pair_prefix[G] = run_pair;
+            gu_prefix[G] = run[0];
+            dn_prefix[G] = run[1];
+            tile_prefix[G] = run[2];
+            mid_prefix[G] = run[3];
+            pair_prefix[G] = run[4];
+            xcol_prefix[G] = run[5];
             for (int i = 0; i < kJobSlots; ++i) {
                 mbar_init(&jfull[i], 1);
-                mbar_init(&jempty[i], 15);
+                mbar_init(&jempty[i], 1 + kIssuers + 8 + 4);  // stager, issuers, dequant, epilogue warps
             }
             for (int i = 0; i < kRawStages; ++i) {
                 mbar_init(&rfull[i], 1);
@@ -242,21 +262,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
             }
             for (int i = 0; i < kASlots; ++i) {
                 mbar_init(&afull[i], 8);
-                mbar_init(&aempty[i], 1);
+                mbar_init(&aempty[i], kIssuers);
             }
             for (int i = 0; i < kBStages; ++i) {
-                mbar_init(&bfull[i], 2);
-                mbar_init(&bempty[i], 1);
+                mbar_init(&bfull[i], 1);
+                mbar_init(&bempty[i], kIssuers);
             }
             for (int i = 0; i < 2; ++i) {
-                mbar_init(&dfull[i], 1);
+                mbar_init(&dfull[i], kIssuers);
                 mbar_init(&dempty[i], 4);
             }
-            mbar_init(drain, 1);
+            for (int i = 0; i < kIssuers; ++i) mbar_init(&drain[i], 1);
             *abort_flag = 0;
             int dph_total = 0;  // down jobs that write one 256-row output tile
-            for (int g = 0; g < G; ++g)
-                dph_total += ((gn[g] + kNt - 1) / kNt) * tc_nkc_dn(gexp[g] < 0 ? p.Is : p.I, T);
+            for (int g = 0; g < G; ++g) {
+                const bool sh = gexp[g] < 0;
+                const int nt = tc_nt(sh ? p.shared.fmt : p.routed.fmt);
+                dph_total += ((gn[g] + nt - 1) / nt) * tc_nkc_dn(sh ? p.Is : p.I, T);
+            }
             *dn_per_ht_s = dph_total;
             fence_mbar_init();
         }
@@ -270,7 +293,46 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
     const int njobs = NGU + NDN;
     const int dn_per_ht = *dn_per_ht_s;
 
-    // read one job descriptor from the ring (all threads of a role)
+    // ---- this CTA's share of the activation columns -> f16 B tiles --------
+    // Column c goes to CTA c mod grid; every 128-K unit of its x row is
+    // converted once into the (group, column tile)'s B layout in global memory.
+    {
+        const int U = tab.U();
+        uint32_t range_bad = 0;
+        for (int c = blockIdx.x; c < U; c += gridDim.x) {
+            const int g = group_of_col(g0, G, c);
+            const int nt = tc_nt(gexp[g] < 0 ? p.shared.fmt : p.routed.fmt);
+            const int ct = (c - g0[g]) / nt, cl = (c - g0[g]) % nt;
+            const int n = min(nt, gn[g] - ct * nt), npad = ((n + 15) / 16) * 16;
+            uint8_t *base = p.xB + ((long long)xcol_prefix[g] + (long long)ct * nt) * H * 2;
+            const __nv_bfloat16 *xr = p.x + (size_t)crow[c] * H;
+            for (int it = tid; it < H / 8; it += kTcThreads) {
+                const int ku = it >> 4, k8 = it & 15;
+                const uint4 q = __ldg(reinterpret_cast<const uint4 *>(xr + it * 8));
+                const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+                uint32_t o[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const __half2 h = __floats2half2_rn(bf16_bits_to_float(w4[k] & 0xffffu),
+                                                        bf16_bits_to_float(w4[k] >> 16));
+                    if (__hisinf(__low2half(h)) || __hisinf(__high2half(h))) range_bad = 1;
+                    o[k] = pack_h2(h);
+                }
+                *reinterpret_cast<uint4 *>(base + (long long)ku * npad * 256 + b_off(cl, k8 * 8)) =
+                    make_uint4(o[0], o[1], o[2], o[3]);
+            }
+        }
+        if (range_bad) atomicOr(err, kErrRange);
+        __threadfence();
+        __syncthreads();
+        if (tid == 0)
+            for (int c = blockIdx.x; c < U; c += gridDim.x) {
+                const int g = group_of_col(g0, G, c);
+                const int nt = tc_nt(gexp[g] < 0 ? p.shared.fmt : p.routed.fmt);
+                atom_add_acq_rel_gpu(p.x_ready + pair_prefix[g] + (c - g0[g]) / nt, 1u);
+            }
+    }
+
     auto job_at = [&](int slot) -> TcJob { return jobs[slot]; };
 
     if (warp == 0) {
@@ -282,9 +344,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
             for (;;) {
                 TcJob d;
                 const int j = (int)atomicAdd(&p.hdr->job_next, 1u);
-                if (*abort_flag) d.kind = -1;
-                else if (j >= njobs) d.kind = -1;
-                else {
+                if (*abort_flag || j >= njobs) {
+                    d.kind = -1;
+                } else {
                     const bool gu = j < NGU;
                     int g, local;
                     if (gu) {
@@ -304,6 +366,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                     d.fmt = sh ? p.shared.fmt : p.routed.fmt;
                     d.Ig = sh ? p.Is : p.I;
                     const int tiles = d.Ig / 128;
+                    const int nt = tc_nt(d.fmt);
                     if (gu) {
                         d.kind = 0;
                         d.nkc = tc_nkc_gu(d.fmt, H, T);
@@ -331,12 +394,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                         d.rows0 = d.tile * 256;
                         d.rows1 = d.tile * 256 + 128;
                     }
-                    d.n = min(kNt, gn[g] - d.ct * kNt);
+                    d.n = min(nt, gn[g] - d.ct * nt);
                     d.npad = ((d.n + 15) / 16) * 16;
-                    d.col0 = g0[g] + d.ct * kNt;
+                    d.col0 = g0[g] + d.ct * nt;
                     d.tile_id = tile_prefix[g] + d.ct * tiles + (d.kind == 0 ? d.tile : 0);
                     d.pair = pair_prefix[g] + d.ct;
-                    d.mid_off = ((long long)mid_prefix[g] + (long long)d.ct * tiles * kNt) * 512ll;
+                    d.mid_off = ((long long)mid_prefix[g] + (long long)d.ct * tiles * nt) * 256ll;
+                    d.x_off = ((long long)xcol_prefix[g] + (long long)d.ct * nt) * H * 2;
                 }
                 if (!mbar_wait(&jempty[js], jph ^ 1, abort_flag, err)) break;
                 jobs[js] = d;
@@ -395,8 +459,69 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
             }
         }
     } else if (warp == 1) {
-        // ===================== MMA issuer =====================
+        // ===================== B stager =====================
+        int js = 0, jph = 0, bs = 0, bph = 0;
+        for (;;) {
+            if (!__all_sync(0xffffffffu, mbar_wait(&jfull[js], jph, abort_flag, err))) break;
+            const TcJob d = job_at(js);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&jempty[js]);
+            if (++js == kJobSlots) {
+                js = 0;
+                jph ^= 1;
+            }
+            if (d.kind < 0) break;
+            // wait until the B operand's producers are done: the converted
+            // activation columns (gate/up) or every quarter of every row tile
+            // of the group's intermediate (down)
+            int okl = 1;
+            if (lane == 0) {
+                const uint32_t need = d.kind == 0 ? (uint32_t)d.n : (uint32_t)(4 * (d.Ig / 128));
+                const uint32_t *flag = (d.kind == 0 ? p.x_ready : p.group_ready) + d.pair;
+                if (ld_acquire_gpu(flag) < need) {
+                    const unsigned long long t0 = globaltimer_ns();
+                    while (ld_acquire_gpu(flag) < need) {
+                        if (*abort_flag) {
+                            okl = 0;
+                            break;
+                        }
+                        if (globaltimer_ns() - t0 > kWaitBudgetNs) {
+                            atomicOr(err, kErrWaitTimeout);
+                            *abort_flag = 1;
+                            okl = 0;
+                            break;
+                        }
+                        __nanosleep(64);
+                    }
+                }
+                // generic-proxy writes of other CTAs (acquired above) before the
+                // async-proxy reads below
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+            }
+            bool ok = __shfl_sync(0xffffffffu, okl, 0) != 0;
+            const uint32_t bytes = (uint32_t)d.npad * 256u;
+            const uint8_t *src0 = d.kind == 0 ? p.xB + d.x_off : p.midB + d.mid_off;
+            for (int u = 0; u < d.nunits && ok; ++u) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&bempty[bs], bph ^ 1, abort_flag, err))) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    const int ku = d.k0 / kUnitK + u;  // global K unit index
+                    mbar_arrive_expect_tx(&bfull[bs], bytes);
+                    bulk_load(bbuf + bs * kBStageBytes, src0 + (long long)ku * bytes, bytes, &bfull[bs]);
+                }
+                if (++bs == kBStages) {
+                    bs = 0;
+                    bph ^= 1;
+                }
+            }
+            if (!ok) break;
+        }
+    } else if (warp < 2 + kIssuers) {
+        // ===================== MMA issuers (warps 2-5) =====================
         if (lane == 0) {
+            const int q = warp - 2, tile = q & 1, kh = q >> 1;
             int js = 0, jph = 0, as = 0, aph = 0, bs = 0, bph = 0, ds = 0, dph = 0;
             bool issued = false;
             for (;;) {
@@ -418,20 +543,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                     if (ok && !mbar_wait(&bfull[bs], bph, abort_flag, err)) ok = false;
                     if (!ok) break;
                     tc_fence_after();
-                    const uint32_t a0 = tmem + as * 128, a1 = a0 + 64;
-                    const uint32_t d0 = tmem + kDCol + ds * 64, d1 = d0 + 32;
+                    const uint32_t a = tmem + as * 128 + tile * 64;
+                    const uint32_t dd = tmem + kDCol + ds * 128 + (tile * 2 + kh) * 32;
                     const uint32_t bb = smem_u32(bbuf + bs * kBStageBytes);
-#pragma unroll 1
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const bool acc = !(fresh && ks == 0);
-                        const uint64_t bh = smem_desc_noswz(bb + ks * 256, 128, 2048);
-                        mma_f16_ats(d0, a0 + ks * 8, bh, idesc, acc);
-                        mma_f16_ats(d1, a1 + ks * 8, bh, idesc, acc);
-                        if (d.kind == 1) {
-                            const uint64_t bl = smem_desc_noswz(bb + d.npad * 256 + ks * 256, 128, 2048);
-                            mma_f16_ats(d0, a0 + ks * 8, bl, idesc, true);
-                            mma_f16_ats(d1, a1 + ks * 8, bl, idesc, true);
-                        }
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int ks = kh * 4 + k;
+                        mma_f16_ats(dd, a + ks * 8, smem_desc_noswz(bb + ks * 256, 128, 2048), idesc,
+                                    !(fresh && k == 0));
                     }
                     issued = true;
                     mma_commit(&aempty[as]);
@@ -454,113 +573,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                 }
                 if (!ok) break;
             }
-            if (issued) {  // all MMAs retired before TMEM is released
-                mma_commit(drain);
+            if (issued) {  // all of this thread's MMAs retired before TMEM is released
+                mma_commit(&drain[q]);
                 const unsigned long long t0 = globaltimer_ns();
-                while (!mbar_try_wait(drain, 0) && globaltimer_ns() - t0 < kWaitBudgetNs) {
+                while (!mbar_try_wait(&drain[q], 0) && globaltimer_ns() - t0 < kWaitBudgetNs) {
                 }
             }
         }
-    } else if (warp < 4) {
-        // ===================== B stagers (warps 2-3) =====================
-        // Each warp decides alone (lane votes), so an aborted wait never
-        // leaves a warp waiting at a barrier for another.
-        const int st = tid - 64;
-        int js = 0, jph = 0, bs = 0, bph = 0;
-        for (;;) {
-            if (!__all_sync(0xffffffffu, mbar_wait(&jfull[js], jph, abort_flag, err))) break;
-            const TcJob d = job_at(js);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&jempty[js]);
-            if (++js == kJobSlots) {
-                js = 0;
-                jph ^= 1;
-            }
-            if (d.kind < 0) break;
-            bool ok = true;
-            if (d.kind == 1 && warp == 2) {
-                // the group's intermediate must be complete: every row tile, every quarter
-                int okl = 1;
-                if (lane == 0) {
-                    const uint32_t need = (uint32_t)(4 * (d.Ig / 128));
-                    const uint32_t *flag = p.group_ready + d.pair;
-                    if (ld_acquire_gpu(flag) < need) {
-                        const unsigned long long t0 = globaltimer_ns();
-                        while (ld_acquire_gpu(flag) < need) {
-                            if (*abort_flag) {
-                                okl = 0;
-                                break;
-                            }
-                            if (globaltimer_ns() - t0 > kWaitBudgetNs) {
-                                atomicOr(err, kErrWaitTimeout);
-                                *abort_flag = 1;
-                                okl = 0;
-                                break;
-                            }
-                            __nanosleep(128);
-                        }
-                    }
-                }
-                ok = __shfl_sync(0xffffffffu, okl, 0) != 0;
-            }
-            for (int u = 0; u < d.nunits && ok; ++u) {
-                if (!__all_sync(0xffffffffu, mbar_wait(&bempty[bs], bph ^ 1, abort_flag, err))) {
-                    ok = false;
-                    break;
-                }
-                uint8_t *dst = bbuf + bs * kBStageBytes;
-                const int ku = d.k0 / kUnitK + u;  // global K unit index
-                if (d.kind == 1) {
-                    if (lane == 0) {
-                        if (warp == 2) {
-                            // generic-proxy writes by other CTAs (acquired above) before
-                            // this async-proxy read
-                            asm volatile("fence.proxy.async.global;" ::: "memory");
-                            const uint32_t bytes = (uint32_t)d.npad * 512u;
-                            mbar_arrive_expect_tx(&bfull[bs], bytes);
-                            bulk_load(dst, p.midB + d.mid_off + (long long)ku * d.npad * 512, bytes, &bfull[bs]);
-                        } else {
-                            mbar_arrive(&bfull[bs]);
-                        }
-                    }
-                } else {
-                    // gather x columns, bf16 -> f16, core-matrix layout
-                    uint32_t range_bad = 0;
-                    for (int it = st; it < d.npad * 16; it += 64) {
-                        const int c = it >> 4, k8 = it & 15;
-                        uint4 v = make_uint4(0, 0, 0, 0);
-                        if (c < d.n) {
-                            const int t = crow[d.col0 + c];
-                            const uint4 q = __ldg(reinterpret_cast<const uint4 *>(
-                                p.x + (size_t)t * H + ku * kUnitK + k8 * 8));
-                            const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
-                            uint32_t o[4];
-#pragma unroll
-                            for (int k = 0; k < 4; ++k) {
-                                const __half2 h = __floats2half2_rn(bf16_bits_to_float(w4[k] & 0xffffu),
-                                                                    bf16_bits_to_float(w4[k] >> 16));
-                                if (__hisinf(__low2half(h)) || __hisinf(__high2half(h))) range_bad = 1;
-                                o[k] = pack_h2(h);
-                            }
-                            v = make_uint4(o[0], o[1], o[2], o[3]);
-                        }
-                        *reinterpret_cast<uint4 *>(dst + b_off(c, k8 * 8)) = v;
-                    }
-                    if (range_bad) atomicOr(err, kErrRange);
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&bfull[bs]);
-                }
-                if (++bs == kBStages) {
-                    bs = 0;
-                    bph ^= 1;
-                }
-            }
-            if (!ok) break;
-        }
-    } else if (warp < 12) {
-        // ===================== dequant (tile0: warps 4-7, tile1: 8-11) =====================
-        const int wg = (warp - 4) >> 2;
+    } else if (warp < 2 + kIssuers + 8) {
+        // ===================== dequant (tile0: warps 6-9, tile1: 10-13) =====================
+        const int wg = (warp - 6) >> 2;
         const int r = ((warp & 3) << 5) | lane;  // row of the tile == TMEM lane
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         int js = 0, jph = 0, rs = 0, rph = 0, as = 0, aph = 0;
@@ -648,7 +670,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
             if (!ok) break;
         }
     } else {
-        // ===================== epilogue (warps 12-15) =====================
+        // ===================== epilogue (warps 14-17) =====================
         // Each warp owns 32 rows of the tile (its TMEM lane quarter) and runs
         // the reductions for those rows on its own: counters are kept per
         // (tile, quarter), so no warp ever waits for another.
@@ -668,46 +690,98 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
             if (d.kind < 0) break;
             const bool fp8 = d.fmt == kFmtFp8B128;
             const WeightsDev &W = d.shared ? p.shared : p.routed;
-            float acc0[kNt], acc1[kNt];
+            const int i = d.tile * 128 + r;                      // gate/up: intermediate row
+            const int h0 = d.rows0 + r, h1 = d.rows1 + r;        // down: output rows
+            const float gs13 = (d.kind == 0 && !fp8) ? __ldg(W.w13_gscale + d.e) : 1.0f;
+            uint8_t *mb = p.midB + d.mid_off + (long long)d.tile * d.npad * 256;
+            uint32_t range_bad = 0;
+
+            // phase 1, per 16-column chunk: the chunk's (gate, up) or (row h0, row h1)
+            // values -> partial sums, the intermediate, or the per-chunk down output
+            auto emit = [&](int cb, const float (&v0)[16], const float (&v1)[16]) {
 #pragma unroll
-            for (int c = 0; c < kNt; ++c) acc0[c] = acc1[c] = 0.0f;
-            const int nacc = fp8 ? d.nunits : 1;
-            bool ok = true;
-            for (int a = 0; a < nacc; ++a) {
-                if (!__all_sync(0xffffffffu, mbar_wait(&dfull[ds], dph, abort_flag, err))) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t dcol = tmem + lane_base + kDCol + ds * 64;
-                float s0 = 1.0f, s1 = 1.0f;
-                if (fp8) {
-                    const int ku = d.k0 / kUnitK + a;  // 128-K block index along the input dim
-                    const float *sc = reinterpret_cast<const float *>(d.kind == 0 ? W.w13_scale : W.w2_scale);
-                    const int rows = d.kind == 0 ? 2 * d.Ig : H;
-                    const int cols_blk = (d.kind == 0 ? H : d.Ig) / 128;
-                    const size_t base = (size_t)d.e * (rows / 128);
-                    s0 = __ldg(sc + (base + d.rows0 / 128) * cols_blk + ku);
-                    s1 = (d.rows1 < rows) ? __ldg(sc + (base + d.rows1 / 128) * cols_blk + ku) : 0.0f;
-                }
-#pragma unroll
-                for (int cb = 0; cb < kNt; cb += 16) {
-                    if (cb < d.npad) {
-                        uint32_t v0[16], v1[16];
-                        tmem_ld16(dcol + cb, v0);
-                        tmem_ld16(dcol + 32 + cb, v1);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            if (fp8) {
-                                acc0[cb + j] = __fmaf_rn(s0, __uint_as_float(v0[j]), acc0[cb + j]);
-                                acc1[cb + j] = __fmaf_rn(s1, __uint_as_float(v1[j]), acc1[cb + j]);
-                            } else {
-                                acc0[cb + j] = __uint_as_float(v0[j]);
-                                acc1[cb + j] = __uint_as_float(v1[j]);
-                            }
+                for (int j = 0; j < 16; ++j) {
+                    const int c = cb + j;
+                    if (c >= d.n) continue;
+                    const size_t col = (size_t)(d.col0 + c);
+                    if (d.kind == 0) {
+                        if (d.nkc > 1) {
+                            p.P[(((size_t)d.kc * 2 + 0) * p.Ucap + col) * p.Imax + i] = v0[j];
+                            p.P[(((size_t)d.kc * 2 + 1) * p.Ucap + col) * p.Imax + i] = v1[j];
+                        } else {
+                            const float m = __fmul_rn(silu_f32(__fmul_rn(v0[j], gs13)), __fmul_rn(v1[j], gs13));
+                            const __half hm = __float2half_rn(m);
+                            if (__hisinf(hm) || !(fabsf(m) == fabsf(m))) range_bad = 1;
+                            *reinterpret_cast<__half *>(mb + b_off(c, r)) = hm;
                         }
+                    } else {
+                        float *y = p.Y + ((size_t)d.kc * p.Ucap + col) * H;
+                        if (h0 < H) y[h0] = v0[j];
+                        if (h1 < H) y[h1] = v1[j];
                     }
+                }
+            };
+
+            bool ok = true;
+            if (fp8) {
+                // per 128-K unit: fresh accumulators, fp32 block scale, running sum
+                float acc0[16], acc1[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) acc0[j] = acc1[j] = 0.0f;
+                const float *sc = reinterpret_cast<const float *>(d.kind == 0 ? W.w13_scale : W.w2_scale);
+                const int rows = d.kind == 0 ? 2 * d.Ig : H;
+                const int cols_blk = (d.kind == 0 ? H : d.Ig) / 128;
+                const size_t sbase = (size_t)d.e * (rows / 128);
+                for (int u = 0; u < d.nunits; ++u) {
+                    if (!__all_sync(0xffffffffu, mbar_wait(&dfull[ds], dph, abort_flag, err))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const int ku = d.k0 / kUnitK + u;
+                    const float s0 = __ldg(sc + (sbase + d.rows0 / 128) * cols_blk + ku);
+                    const float s1 = (d.rows1 < rows) ? __ldg(sc + (sbase + d.rows1 / 128) * cols_blk + ku) : 0.0f;
+                    const uint32_t dcol = tmem + lane_base + kDCol + ds * 128;
+                    uint32_t a0[16], a1[16], b0[16], b1[16];
+                    tmem_ld16(dcol + 0, a0);
+                    tmem_ld16(dcol + 32, a1);
+                    tmem_ld16(dcol + 64, b0);
+                    tmem_ld16(dcol + 96, b1);
+                    tmem_wait_ld();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&dempty[ds]);
+                    if (++ds == 2) {
+                        ds = 0;
+                        dph ^= 1;
+                    }
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        acc0[j] = __fmaf_rn(s0, __fadd_rn(__uint_as_float(a0[j]), __uint_as_float(a1[j])), acc0[j]);
+                        acc1[j] = __fmaf_rn(s1, __fadd_rn(__uint_as_float(b0[j]), __uint_as_float(b1[j])), acc1[j]);
+                    }
+                }
+                if (!ok) break;
+                emit(0, acc0, acc1);
+            } else {
+                if (!__all_sync(0xffffffffu, mbar_wait(&dfull[ds], dph, abort_flag, err))) break;
+                tc_fence_after();
+                const uint32_t dcol = tmem + lane_base + kDCol + ds * 128;
+#pragma unroll 1
+                for (int cb = 0; cb < d.npad; cb += 16) {
+                    uint32_t a0[16], a1[16], b0[16], b1[16];
+                    tmem_ld16(dcol + cb, a0);
+                    tmem_ld16(dcol + 32 + cb, a1);
+                    tmem_ld16(dcol + 64 + cb, b0);
+                    tmem_ld16(dcol + 96 + cb, b1);
+                    tmem_wait_ld();
+                    float v0[16], v1[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        v0[j] = __fadd_rn(__uint_as_float(a0[j]), __uint_as_float(a1[j]));
+                        v1[j] = __fadd_rn(__uint_as_float(b0[j]), __uint_as_float(b1[j]));
+                    }
+                    emit(cb, v0, v1);
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -717,88 +791,51 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                     dph ^= 1;
                 }
             }
-            if (!ok) break;
 
             if (d.kind == 0) {
-                // ---- gate/up: partial sums, the last chunk reduces, SwiGLU ----
-                const int i = d.tile * 128 + r;  // intermediate row
-                bool last = true;
+                // ---- gate/up phase 2: the last K chunk reduces in kc order, SwiGLU ----
+                bool have_mid = d.nkc == 1;
                 if (d.nkc > 1) {
-#pragma unroll
-                    for (int c = 0; c < kNt; ++c)
-                        if (c < d.n) {
-                            const size_t col = (size_t)(d.col0 + c);
-                            p.P[(((size_t)d.kc * 2 + 0) * p.Ucap + col) * p.Imax + i] = acc0[c];
-                            p.P[(((size_t)d.kc * 2 + 1) * p.Ucap + col) * p.Imax + i] = acc1[c];
-                        }
                     __threadfence();
                     __syncwarp();
                     int l = 0;
                     if (lane == 0)
                         l = atom_add_acq_rel_gpu(p.tile_cnt + (size_t)d.tile_id * 4 + quarter, 1u) ==
                             (uint32_t)d.nkc - 1;
-                    last = __shfl_sync(0xffffffffu, l, 0) != 0;
-                    if (last) {
+                    if (__shfl_sync(0xffffffffu, l, 0)) {
                         __threadfence();
-#pragma unroll
-                        for (int c = 0; c < kNt; ++c)
-                            if (c < d.n) {
-                                const size_t col = (size_t)(d.col0 + c);
-                                float sg = __ldcg(p.P + ((size_t)0 * p.Ucap + col) * p.Imax + i);
-                                float su = __ldcg(p.P + ((size_t)1 * p.Ucap + col) * p.Imax + i);
-                                for (int kc = 1; kc < d.nkc; ++kc) {
-                                    sg = __fadd_rn(sg, __ldcg(p.P + (((size_t)kc * 2 + 0) * p.Ucap + col) * p.Imax + i));
-                                    su = __fadd_rn(su, __ldcg(p.P + (((size_t)kc * 2 + 1) * p.Ucap + col) * p.Imax + i));
-                                }
-                                acc0[c] = sg;
-                                acc1[c] = su;
+                        for (int c = 0; c < d.n; ++c) {
+                            const size_t col = (size_t)(d.col0 + c);
+                            float sg = __ldcg(p.P + ((size_t)0 * p.Ucap + col) * p.Imax + i);
+                            float su = __ldcg(p.P + ((size_t)1 * p.Ucap + col) * p.Imax + i);
+                            for (int kc = 1; kc < d.nkc; ++kc) {
+                                sg = __fadd_rn(sg, __ldcg(p.P + (((size_t)kc * 2 + 0) * p.Ucap + col) * p.Imax + i));
+                                su = __fadd_rn(su, __ldcg(p.P + (((size_t)kc * 2 + 1) * p.Ucap + col) * p.Imax + i));
                             }
+                            const float m = __fmul_rn(silu_f32(__fmul_rn(sg, gs13)), __fmul_rn(su, gs13));
+                            const __half hm = __float2half_rn(m);
+                            if (__hisinf(hm) || !(fabsf(m) == fabsf(m))) range_bad = 1;
+                            *reinterpret_cast<__half *>(mb + b_off(c, r)) = hm;
+                        }
                         if (lane == 0) p.tile_cnt[(size_t)d.tile_id * 4 + quarter] = 0;
+                        have_mid = true;
                     }
                 }
-                if (last) {
-                    const float gs = (d.fmt == kFmtNvfp4) ? __ldg(W.w13_gscale + d.e) : 1.0f;
-                    uint8_t *mb = p.midB + d.mid_off + (long long)d.tile * d.npad * 512;
-                    uint32_t range_bad = 0;
-#pragma unroll
-                    for (int c = 0; c < kNt; ++c)
-                        if (c < d.npad) {
-                            __half hi = __float2half_rn(0.0f), lo = hi;
-                            if (c < d.n) {
-                                const float g = (d.fmt == kFmtNvfp4) ? __fmul_rn(acc0[c], gs) : acc0[c];
-                                const float u = (d.fmt == kFmtNvfp4) ? __fmul_rn(acc1[c], gs) : acc1[c];
-                                const float m = __fmul_rn(silu_f32(g), u);
-                                hi = __float2half_rn(m);
-                                lo = __float2half_rn(__fsub_rn(m, __half2float(hi)));
-                                if (__hisinf(hi) || !(fabsf(m) == fabsf(m))) range_bad = 1;
-                            }
-                            *reinterpret_cast<__half *>(mb + b_off(c, r)) = hi;
-                            *reinterpret_cast<__half *>(mb + d.npad * 256 + b_off(c, r)) = lo;
-                        }
-                    if (range_bad) atomicOr(err, kErrRange);
+                if (range_bad) atomicOr(err, kErrRange);
+                if (have_mid) {
                     __threadfence();
                     __syncwarp();
                     if (lane == 0) atom_add_acq_rel_gpu(p.group_ready + d.pair, 1u);
                 }
             } else {
-                // ---- down: per-chunk outputs; the last job on a 256-row tile combines ----
-                const int h0 = d.rows0 + r, h1 = d.rows1 + r;
-#pragma unroll
-                for (int c = 0; c < kNt; ++c)
-                    if (c < d.n) {
-                        const size_t col = (size_t)(d.col0 + c);
-                        float *y = p.Y + ((size_t)d.kc * p.Ucap + col) * H;
-                        if (h0 < H) y[h0] = acc0[c];
-                        if (h1 < H) y[h1] = acc1[c];
-                    }
+                // ---- down phase 2: the last job on a 256-row tile combines ----
                 __threadfence();
                 __syncwarp();
                 int l = 0;
                 if (lane == 0)
                     l = atom_add_acq_rel_gpu(p.htile_cnt + (size_t)d.tile * 4 + quarter, 1u) ==
                         (uint32_t)dn_per_ht - 1;
-                const bool last = __shfl_sync(0xffffffffu, l, 0) != 0;
-                if (last) {
+                if (__shfl_sync(0xffffffffu, l, 0)) {
                     __threadfence();
                     const int nkc_s = tc_nkc_dn(p.Is, T), nkc_r = tc_nkc_dn(p.I, T);
                     const float gs_s = p.shared.fmt == kFmtNvfp4 ? __ldg(p.shared.w2_gscale) : 1.0f;
@@ -847,7 +884,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
         __threadfence();
         if (atom_add_acq_rel_gpu(&p.hdr->exit_cnt, 1u) == gridDim.x - 1) {
             // every CTA is done with the counters: leave them zero for the next launch
-            for (int i = 0; i < pair_prefix[G]; ++i) p.group_ready[i] = 0;
+            for (int i = 0; i < pair_prefix[G]; ++i) {
+                p.group_ready[i] = 0;
+                p.x_ready[i] = 0;
+            }
             p.hdr->job_next = 0;
             __threadfence();
             p.hdr->exit_cnt = 0;
