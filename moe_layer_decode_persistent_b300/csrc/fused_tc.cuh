@@ -17,10 +17,11 @@
 //     tile0 = rows ht*256.., tile1 = rows ht*256+128.., K = I chunk
 // Both tiles of a job share the B operand (the group's activation columns).
 //
-// Per CTA the roles are warp-specialised (18 warps):
+// Per CTA the roles are warp-specialised (26 warps):
 //   warp 0      producer: claims jobs, TMA-loads 128-byte-wide weight boxes
 //               (SWIZZLE_128B) and NVFP4 block scales into a 3-stage ring
-//   warp 1      B stager: bulk-copies the job's B tile per 128-K unit, the
+//   warp 1      B stager: copies the job's B tile per 128-K unit with
+//               cp.async (not the TMA queue, which is full of weight boxes), the
 //               f16 activation columns (gate/up; converted once per launch in
 //               the prologue, spread over all CTAs) or the f16 intermediate
 //               (down), after waiting for its producers
@@ -29,11 +30,12 @@
 //               one MMA per ~120 cycles whatever N is, so four issuers split
 //               each unit: issuer q takes tile q&1, K-steps of half q>>1, into
 //               its own accumulator (the halves are added in a fixed order)
-//   warps 6-9   dequant of tile0, warps 10-13 dequant of tile1: one thread per
-//               weight row, E2M1*E4M3 -> exact f16 (or E4M3 -> f16), written
-//               to TMEM as the MMA's A operand (the weights never touch
-//               shared memory as f16)
-//   warps 14-17 epilogue: TMEM accumulators -> registers; FP8 128x128 block
+//   warps 6-21  dequant, four warpgroups (tile x unit parity), ping-ponged so
+//               one pair converts while the other synchronises: one thread
+//               per weight row, E2M1*E4M3 -> exact f16 (or E4M3 -> f16),
+//               written to TMEM as the MMA's A operand (the weights never
+//               touch shared memory as f16)
+//   warps 22-25 epilogue: TMEM accumulators -> registers; FP8 128x128 block
 //               scales applied per 128-K block in fp32; partial sums, the
 //               fixed-order reductions, SwiGLU, the f16 intermediate, and the
 //               final combine + single bf16 write
@@ -53,10 +55,11 @@
 
 namespace moe {
 
-constexpr int kTcThreads = 576;
+constexpr int kTcThreads = 832;
+constexpr int kDqWarps = 16;
 constexpr int kTcMaxT = 64;
-constexpr int kNt = 32;               // columns per job at most (NVFP4)
-constexpr int kNtFp8 = 16;            // FP8 jobs: fp32 block-scale promotion in registers
+constexpr int kNt = 32;               // columns per job at most (NVFP4, T > 16)
+constexpr int kNtSmall = 16;          // columns per job when T <= 16, and for FP8 jobs
 constexpr int kUnitK = 128;           // K elements of one TMEM A unit per tile
 constexpr int kRawStages = 4;
 constexpr int kRawTileBytes = 16384;  // 128 rows x 128 bytes
@@ -64,12 +67,18 @@ constexpr int kRawScaleOff = 2 * kRawTileBytes;
 constexpr int kRawStageBytes = 2 * kRawTileBytes + 2 * 2048;  // + NVFP4 scales
 constexpr int kBStages = 4;
 constexpr int kBStageBytes = kNt * kUnitK * 2;  // f16 [32][128]
-constexpr int kASlots = 2;
+constexpr int kASlotsMax = 3;         // TMEM A slots: 3 when jobs have 16 columns, else 2
 constexpr int kIssuers = 4;
 constexpr int kJobSlots = 4;
 constexpr int kTmemCols = 512;
-constexpr int kDCol = kASlots * 128;  // two D sets of 4 x 32 columns follow
-__host__ __device__ constexpr int tc_nt(int fmt) { return fmt == kFmtFp8B128 ? kNtFp8 : kNt; }
+// Columns per job. Depends on the launch (T) and the format only, never on a
+// group's size, so the dedup and one-row forms split work the same way.
+__host__ __device__ constexpr int tc_nt(int fmt, int T) {
+    return (fmt == kFmtFp8B128 || T <= 16) ? kNtSmall : kNt;
+}
+// TMEM: nA A slots of 128 columns, then two D sets of 4 x ntmax columns.
+__host__ __device__ constexpr int tc_ntmax(int T) { return T <= 16 ? kNtSmall : kNt; }
+__host__ __device__ constexpr int tc_aslots(int T) { return T <= 16 ? 3 : 2; }
 constexpr int kKcNvfp4 = 1792;
 constexpr int kKcFp8 = 1024;
 constexpr int kKcDown = 1024;
@@ -138,9 +147,8 @@ struct TcSmem {
     static constexpr int bbuf = raw + kRawStages * kRawStageBytes;
     static constexpr int jobs = bbuf + kBStages * kBStageBytes;
     static constexpr int bars = jobs + kJobSlots * (int)sizeof(TcJob);
-    // jfull, jempty, rfull, rempty, afull, aempty, bfull, bempty, dfull, dempty, drain[4]
-    static constexpr int nbars =
-        2 * kJobSlots + 2 * kRawStages + 2 * kASlots + 2 * kBStages + 2 * 2 + kIssuers;
+    // jfull, jempty, rfull, rempty, sfull, sempty, dfull, dempty, drain[4]
+    static constexpr int nbars = 2 * kJobSlots + 2 * kRawStages + 2 * kASlotsMax + 2 * 2 + kIssuers;
     static constexpr int misc = bars + nbars * 8;  // tmem addr, abort, flags
     static constexpr int tables = misc + 64;       // group table, then per-group arrays
 };
@@ -171,6 +179,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int T = p.T, K = p.K, H = p.H;
     const bool no_dedup = (p.flags & kFlagNoDedup) != 0;
+    const int nA = tc_aslots(T), ntmax = tc_ntmax(T);
+    const int dcol0 = nA * 128, dset = 4 * ntmax;  // TMEM D set base and size
 
     uint8_t *raw = smem + TcSmem::raw;
     uint8_t *bbuf = smem + TcSmem::bbuf;
@@ -178,9 +188,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + TcSmem::bars);
     uint64_t *jfull = bars, *jempty = jfull + kJobSlots;
     uint64_t *rfull = jempty + kJobSlots, *rempty = rfull + kRawStages;
-    uint64_t *afull = rempty + kRawStages, *aempty = afull + kASlots;
-    uint64_t *bfull = aempty + kASlots, *bempty = bfull + kBStages;
-    uint64_t *dfull = bempty + kBStages, *dempty = dfull + 2;
+    // a unit slot = one TMEM A slot + one B buffer, filled by the dequant
+    // warps and the B stager together and released by one commit per issuer
+    uint64_t *sfull = rempty + kRawStages, *sempty = sfull + kASlotsMax;
+    uint64_t *dfull = sempty + kASlotsMax, *dempty = dfull + 2;
     uint64_t *drain = dempty + 2;
     uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(smem + TcSmem::misc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + TcSmem::misc + 4);
@@ -211,7 +222,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                 const bool sh = gexp[g] < 0;
                 const int fmt = sh ? p.shared.fmt : p.routed.fmt;
                 const int Ig = sh ? p.Is : p.I;
-                const int nt = tc_nt(fmt);
+                const int nt = tc_nt(fmt, T);
                 const int n = gn[g], nct = (n + nt - 1) / nt;
                 const int tiles = Ig / 128;
                 int np = 0;
@@ -254,19 +265,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
             xcol_prefix[G] = run[5];
             for (int i = 0; i < kJobSlots; ++i) {
                 mbar_init(&jfull[i], 1);
-                mbar_init(&jempty[i], 1 + kIssuers + 8 + 4);  // stager, issuers, dequant, epilogue warps
+                mbar_init(&jempty[i], 1 + kIssuers + kDqWarps + 4);  // stager, issuers, dequant, epilogue
             }
             for (int i = 0; i < kRawStages; ++i) {
                 mbar_init(&rfull[i], 1);
-                mbar_init(&rempty[i], 8);
+                mbar_init(&rempty[i], kDqWarps);
             }
-            for (int i = 0; i < kASlots; ++i) {
-                mbar_init(&afull[i], 8);
-                mbar_init(&aempty[i], kIssuers);
-            }
-            for (int i = 0; i < kBStages; ++i) {
-                mbar_init(&bfull[i], 1);
-                mbar_init(&bempty[i], kIssuers);
+            for (int i = 0; i < kASlotsMax; ++i) {
+                mbar_init(&sfull[i], 8 + 32);  // 8 dequant warps + one cp.async arrival per stager lane
+                mbar_init(&sempty[i], kIssuers);
             }
             for (int i = 0; i < 2; ++i) {
                 mbar_init(&dfull[i], kIssuers);
@@ -277,7 +284,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
             int dph_total = 0;  // down jobs that write one 256-row output tile
             for (int g = 0; g < G; ++g) {
                 const bool sh = gexp[g] < 0;
-                const int nt = tc_nt(sh ? p.shared.fmt : p.routed.fmt);
+                const int nt = tc_nt(sh ? p.shared.fmt : p.routed.fmt, T);
                 dph_total += ((gn[g] + nt - 1) / nt) * tc_nkc_dn(sh ? p.Is : p.I, T);
             }
             *dn_per_ht_s = dph_total;
@@ -301,7 +308,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
         uint32_t range_bad = 0;
         for (int c = blockIdx.x; c < U; c += gridDim.x) {
             const int g = group_of_col(g0, G, c);
-            const int nt = tc_nt(gexp[g] < 0 ? p.shared.fmt : p.routed.fmt);
+            const int nt = tc_nt(gexp[g] < 0 ? p.shared.fmt : p.routed.fmt, T);
             const int ct = (c - g0[g]) / nt, cl = (c - g0[g]) % nt;
             const int n = min(nt, gn[g] - ct * nt), npad = ((n + 15) / 16) * 16;
             uint8_t *base = p.xB + ((long long)xcol_prefix[g] + (long long)ct * nt) * H * 2;
@@ -328,7 +335,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
         if (tid == 0)
             for (int c = blockIdx.x; c < U; c += gridDim.x) {
                 const int g = group_of_col(g0, G, c);
-                const int nt = tc_nt(gexp[g] < 0 ? p.shared.fmt : p.routed.fmt);
+                const int nt = tc_nt(gexp[g] < 0 ? p.shared.fmt : p.routed.fmt, T);
                 atom_add_acq_rel_gpu(p.x_ready + pair_prefix[g] + (c - g0[g]) / nt, 1u);
             }
     }
@@ -366,7 +373,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                     d.fmt = sh ? p.shared.fmt : p.routed.fmt;
                     d.Ig = sh ? p.Is : p.I;
                     const int tiles = d.Ig / 128;
-                    const int nt = tc_nt(d.fmt);
+                    const int nt = tc_nt(d.fmt, T);
                     if (gu) {
                         d.kind = 0;
                         d.nkc = tc_nkc_gu(d.fmt, H, T);
@@ -423,6 +430,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                 const int upst = fp4 ? 2 : 1;
                 const int nst = d.nunits / upst;
                 const int kb0 = fp4 ? d.k0 / 2 : d.k0;
+                const uint64_t pol = l2_evict_first_policy();  // weights are read once
                 bool ok = true;
                 for (int s = 0; s < nst; ++s) {
                     if (!mbar_wait(&rempty[rs], rph ^ 1, abort_flag, err)) {
@@ -432,11 +440,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                     armed &= ~(1u << rs);
                     uint8_t *dst = raw + rs * kRawStageBytes;
                     mbar_arrive_expect_tx(&rfull[rs], fp4 ? kRawStageBytes : 2 * kRawTileBytes);
-                    tma_load_3d(dst, mc, kb0 + s * 128, d.rows0, d.e, &rfull[rs]);
-                    tma_load_3d(dst + kRawTileBytes, mc, kb0 + s * 128, d.rows1, d.e, &rfull[rs]);
+                    tma_load_3d_hint(dst, mc, kb0 + s * 128, d.rows0, d.e, &rfull[rs], pol);
+                    tma_load_3d_hint(dst + kRawTileBytes, mc, kb0 + s * 128, d.rows1, d.e, &rfull[rs], pol);
                     if (fp4) {
-                        tma_load_3d(dst + kRawScaleOff, ms, d.k0 / 16 + s * 16, d.rows0, d.e, &rfull[rs]);
-                        tma_load_3d(dst + kRawScaleOff + 2048, ms, d.k0 / 16 + s * 16, d.rows1, d.e, &rfull[rs]);
+                        tma_load_3d_hint(dst + kRawScaleOff, ms, d.k0 / 16 + s * 16, d.rows0, d.e, &rfull[rs], pol);
+                        tma_load_3d_hint(dst + kRawScaleOff + 2048, ms, d.k0 / 16 + s * 16, d.rows1, d.e,
+                                         &rfull[rs], pol);
                     }
                     armed |= 1u << rs;
                     if (++rs == kRawStages) {
@@ -460,7 +469,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
         }
     } else if (warp == 1) {
         // ===================== B stager =====================
-        int js = 0, jph = 0, bs = 0, bph = 0;
+        int js = 0, jph = 0, bs = 0, bph = 0;  // unit slot ring position
         for (;;) {
             if (!__all_sync(0xffffffffu, mbar_wait(&jfull[js], jph, abort_flag, err))) break;
             const TcJob d = job_at(js);
@@ -494,24 +503,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                         __nanosleep(64);
                     }
                 }
-                // generic-proxy writes of other CTAs (acquired above) before the
-                // async-proxy reads below
-                asm volatile("fence.proxy.async.global;" ::: "memory");
             }
+            // the other lanes' copies below are ordered after lane 0's acquire
             bool ok = __shfl_sync(0xffffffffu, okl, 0) != 0;
+            __syncwarp();
             const uint32_t bytes = (uint32_t)d.npad * 256u;
             const uint8_t *src0 = d.kind == 0 ? p.xB + d.x_off : p.midB + d.mid_off;
             for (int u = 0; u < d.nunits && ok; ++u) {
-                if (!__all_sync(0xffffffffu, mbar_wait(&bempty[bs], bph ^ 1, abort_flag, err))) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&sempty[bs], bph ^ 1, abort_flag, err))) {
                     ok = false;
                     break;
                 }
-                if (lane == 0) {
+                {
                     const int ku = d.k0 / kUnitK + u;  // global K unit index
-                    mbar_arrive_expect_tx(&bfull[bs], bytes);
-                    bulk_load(bbuf + bs * kBStageBytes, src0 + (long long)ku * bytes, bytes, &bfull[bs]);
+                    const uint8_t *src = src0 + (long long)ku * bytes;
+                    uint8_t *dst = bbuf + bs * kBStageBytes;
+                    for (uint32_t o = (uint32_t)lane * 16; o < bytes; o += 32 * 16) cp_async16(dst + o, src + o);
+                    cp_async_arrive_noinc(&sfull[bs]);
                 }
-                if (++bs == kBStages) {
+                if (++bs == nA) {
                     bs = 0;
                     bph ^= 1;
                 }
@@ -522,7 +532,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
         // ===================== MMA issuers (warps 2-5) =====================
         if (lane == 0) {
             const int q = warp - 2, tile = q & 1, kh = q >> 1;
-            int js = 0, jph = 0, as = 0, aph = 0, bs = 0, bph = 0, ds = 0, dph = 0;
+            int js = 0, jph = 0, as = 0, aph = 0, ds = 0, dph = 0;
             bool issued = false;
             for (;;) {
                 if (!mbar_wait(&jfull[js], jph, abort_flag, err)) break;
@@ -539,13 +549,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                 for (int u = 0; u < d.nunits && ok; ++u) {
                     const bool fresh = fp8 || u == 0;
                     if (fresh && !mbar_wait(&dempty[ds], dph ^ 1, abort_flag, err)) ok = false;
-                    if (ok && !mbar_wait(&afull[as], aph, abort_flag, err)) ok = false;
-                    if (ok && !mbar_wait(&bfull[bs], bph, abort_flag, err)) ok = false;
+                    if (ok && !mbar_wait(&sfull[as], aph, abort_flag, err)) ok = false;
                     if (!ok) break;
+                    fence_proxy_async_smem();  // B arrived through the generic proxy (cp.async)
                     tc_fence_after();
                     const uint32_t a = tmem + as * 128 + tile * 64;
-                    const uint32_t dd = tmem + kDCol + ds * 128 + (tile * 2 + kh) * 32;
-                    const uint32_t bb = smem_u32(bbuf + bs * kBStageBytes);
+                    const uint32_t dd = tmem + dcol0 + ds * dset + (tile * 2 + kh) * ntmax;
+                    const uint32_t bb = smem_u32(bbuf + as * kBStageBytes);
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const int ks = kh * 4 + k;
@@ -553,8 +563,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                                     !(fresh && k == 0));
                     }
                     issued = true;
-                    mma_commit(&aempty[as]);
-                    mma_commit(&bempty[bs]);
+                    mma_commit(&sempty[as]);
                     if (fp8 || u == d.nunits - 1) {
                         mma_commit(&dfull[ds]);
                         if (++ds == 2) {
@@ -562,13 +571,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                             dph ^= 1;
                         }
                     }
-                    if (++as == kASlots) {
+                    if (++as == nA) {
                         as = 0;
                         aph ^= 1;
-                    }
-                    if (++bs == kBStages) {
-                        bs = 0;
-                        bph ^= 1;
                     }
                 }
                 if (!ok) break;
@@ -580,12 +585,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                 }
             }
         }
-    } else if (warp < 2 + kIssuers + 8) {
-        // ===================== dequant (tile0: warps 6-9, tile1: 10-13) =====================
-        const int wg = (warp - 6) >> 2;
+    } else if (warp < 2 + kIssuers + kDqWarps) {
+        // ===================== dequant (warps 6-21) =====================
+        // warpgroup dq = (warp - 6) / 4: tile = dq & 1, parity = dq >> 1. A
+        // warpgroup converts its tile's rows of the units whose running index
+        // has its parity; it still steps through every unit and stage so its
+        // ring positions stay in step with the others.
+        const int dq = (warp - 6) >> 2;
+        const int wg = dq & 1, par = dq >> 1;
         const int r = ((warp & 3) << 5) | lane;  // row of the tile == TMEM lane
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-        int js = 0, jph = 0, rs = 0, rph = 0, as = 0, aph = 0;
+        int js = 0, jph = 0, rs = 0, rph = 0, as = 0, aph = 0, ucount = 0;
         for (;;) {
             if (!__all_sync(0xffffffffu, mbar_wait(&jfull[js], jph, abort_flag, err))) break;
             const TcJob d = job_at(js);
@@ -601,35 +611,47 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
             const int nst = d.nunits / upst;
             bool ok = true;
             for (int s = 0; s < nst && ok; ++s) {
+                // every dequant warp waits for every stage, converting or not, so
+                // no warp can arrive on a stage's release twice in one phase
                 if (!__all_sync(0xffffffffu, mbar_wait(&rfull[rs], rph, abort_flag, err))) {
                     ok = false;
                     break;
                 }
-                const uint8_t *tile = raw + rs * kRawStageBytes + wg * kRawTileBytes;
-                const uint8_t *row = tile + r * 128;
+                const uint8_t *row = raw + rs * kRawStageBytes + wg * kRawTileBytes + r * 128;
                 const int sw = r & 7;
-                for (int uu = 0; uu < upst; ++uu) {
-                    if (!__all_sync(0xffffffffu, mbar_wait(&aempty[as], aph ^ 1, abort_flag, err))) {
+                for (int uu = 0; uu < upst; ++uu, ++ucount) {
+                    const int cur = as;
+                    if (++as == nA) {
+                        as = 0;
+                        aph ^= 1;
+                    }
+                    if ((ucount & 1) != par) continue;
+                    const int cur_ph = (as == 0) ? (aph ^ 1) : aph;  // phase of slot `cur`
+                    if (!__all_sync(0xffffffffu, mbar_wait(&sempty[cur], cur_ph ^ 1, abort_flag, err))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t tcol = tmem + lane_base + as * 128 + wg * 64;
+                    const uint32_t tcol = tmem + lane_base + cur * 128 + wg * 64;
                     if (fp4) {
+                        // the unit's 64 code bytes and 8 scale bytes of this row, loaded first
+                        uint4 v[4];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            v[q] = *reinterpret_cast<const uint4 *>(row + (((uu * 4 + q) ^ sw) << 4));
                         const uint2 sc = *reinterpret_cast<const uint2 *>(
                             raw + rs * kRawStageBytes + kRawScaleOff + wg * 2048 + r * 16 + uu * 8);
                         const uint32_t scw[2] = {sc.x, sc.y};
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const int chunk = uu * 4 + q;  // 16 B = 32 codes = 2 scale blocks
-                            const uint4 v = *reinterpret_cast<const uint4 *>(row + ((chunk ^ sw) << 4));
-                            const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
-                            const __half2 s2 = e4m3x2_to_half2((scw[q >> 1] >> (16 * (q & 1))) & 0xffffu);
+                        for (int q = 0; q < 4; ++q) {  // 16 B = 32 codes = 2 scale blocks
+                            const uint32_t vw[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+                            const __half2 s2 = e4m3x2_to_half2(scw[q >> 1] >> (16 * (q & 1)));
                             const __half2 slo = __low2half2(s2), shi = __high2half2(s2);
                             uint32_t o[16];
 #pragma unroll
                             for (int b = 0; b < 16; ++b) {
-                                const __half2 h = e2m1x2_to_half2((vw[b >> 2] >> (8 * (b & 3))) & 0xffu);
+                                // the conversion reads the low byte: no mask needed
+                                const __half2 h = e2m1x2_to_half2(vw[b >> 2] >> (8 * (b & 3)));
                                 o[b] = pack_h2(__hmul2(h, b < 8 ? slo : shi));
                             }
                             tmem_st16(tcol + q * 16, o);
@@ -640,12 +662,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                             uint32_t o[16];
 #pragma unroll
                             for (int hq = 0; hq < 2; ++hq) {
-                                const int chunk = q * 2 + hq;
-                                const uint4 v = *reinterpret_cast<const uint4 *>(row + ((chunk ^ sw) << 4));
-                                const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+                                const uint4 vv = *reinterpret_cast<const uint4 *>(row + (((q * 2 + hq) ^ sw) << 4));
+                                const uint32_t vw[4] = {vv.x, vv.y, vv.z, vv.w};
 #pragma unroll
                                 for (int b = 0; b < 8; ++b)
-                                    o[hq * 8 + b] = pack_h2(e4m3x2_to_half2((vw[b >> 1] >> (16 * (b & 1))) & 0xffffu));
+                                    o[hq * 8 + b] = pack_h2(e4m3x2_to_half2(vw[b >> 1] >> (16 * (b & 1))));
                             }
                             tmem_st16(tcol + q * 16, o);
                         }
@@ -653,11 +674,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                     tmem_wait_st();
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&afull[as]);
-                    if (++as == kASlots) {
-                        as = 0;
-                        aph ^= 1;
-                    }
+                    if (lane == 0) mbar_arrive(&sfull[cur]);
                 }
                 if (!ok) break;
                 __syncwarp();
@@ -741,13 +758,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                     const int ku = d.k0 / kUnitK + u;
                     const float s0 = __ldg(sc + (sbase + d.rows0 / 128) * cols_blk + ku);
                     const float s1 = (d.rows1 < rows) ? __ldg(sc + (sbase + d.rows1 / 128) * cols_blk + ku) : 0.0f;
-                    const uint32_t dcol = tmem + lane_base + kDCol + ds * 128;
-                    uint32_t a0[16], a1[16], b0[16], b1[16];
-                    tmem_ld16(dcol + 0, a0);
-                    tmem_ld16(dcol + 32, a1);
-                    tmem_ld16(dcol + 64, b0);
-                    tmem_ld16(dcol + 96, b1);
-                    tmem_wait_ld();
+                    const uint32_t dcol = tmem + lane_base + dcol0 + ds * dset;
+#pragma unroll
+                    for (int h8 = 0; h8 < 16; h8 += 8) {
+                        uint32_t x0[8], x1[8];
+                        tmem_ld8(dcol + h8, x0);
+                        tmem_ld8(dcol + ntmax + h8, x1);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            acc0[h8 + j] = __fmaf_rn(s0, __fadd_rn(__uint_as_float(x0[j]), __uint_as_float(x1[j])), acc0[h8 + j]);
+                        tmem_ld8(dcol + 2 * ntmax + h8, x0);
+                        tmem_ld8(dcol + 3 * ntmax + h8, x1);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            acc1[h8 + j] = __fmaf_rn(s1, __fadd_rn(__uint_as_float(x0[j]), __uint_as_float(x1[j])), acc1[h8 + j]);
+                    }
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&dempty[ds]);
@@ -755,31 +782,31 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                         ds = 0;
                         dph ^= 1;
                     }
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        acc0[j] = __fmaf_rn(s0, __fadd_rn(__uint_as_float(a0[j]), __uint_as_float(a1[j])), acc0[j]);
-                        acc1[j] = __fmaf_rn(s1, __fadd_rn(__uint_as_float(b0[j]), __uint_as_float(b1[j])), acc1[j]);
-                    }
                 }
                 if (!ok) break;
                 emit(0, acc0, acc1);
             } else {
                 if (!__all_sync(0xffffffffu, mbar_wait(&dfull[ds], dph, abort_flag, err))) break;
                 tc_fence_after();
-                const uint32_t dcol = tmem + lane_base + kDCol + ds * 128;
+                const uint32_t dcol = tmem + lane_base + dcol0 + ds * dset;
 #pragma unroll 1
                 for (int cb = 0; cb < d.npad; cb += 16) {
-                    uint32_t a0[16], a1[16], b0[16], b1[16];
-                    tmem_ld16(dcol + cb, a0);
-                    tmem_ld16(dcol + 32 + cb, a1);
-                    tmem_ld16(dcol + 64 + cb, b0);
-                    tmem_ld16(dcol + 96 + cb, b1);
-                    tmem_wait_ld();
                     float v0[16], v1[16];
+                    {
+                        uint32_t x0[16], x1[16];
+                        tmem_ld16(dcol + cb, x0);
+                        tmem_ld16(dcol + ntmax + cb, x1);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        v0[j] = __fadd_rn(__uint_as_float(a0[j]), __uint_as_float(a1[j]));
-                        v1[j] = __fadd_rn(__uint_as_float(b0[j]), __uint_as_float(b1[j]));
+                        for (int j = 0; j < 16; ++j) v0[j] = __fadd_rn(__uint_as_float(x0[j]), __uint_as_float(x1[j]));
+                    }
+                    {
+                        uint32_t x0[16], x1[16];
+                        tmem_ld16(dcol + 2 * ntmax + cb, x0);
+                        tmem_ld16(dcol + 3 * ntmax + cb, x1);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) v1[j] = __fadd_rn(__uint_as_float(x0[j]), __uint_as_float(x1[j]));
                     }
                     emit(cb, v0, v1);
                 }
