@@ -160,6 +160,7 @@ __host__ __device__ inline int tc_smem_bytes(int T, int K) {
 }
 
 __device__ __forceinline__ uint32_t pack_h2(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
+__device__ __forceinline__ __half2 u32_h2(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
 
 // group of column c: the last g with g0[g] <= c
 __device__ __forceinline__ int group_of_col(const int32_t *g0, int G, int c) {
@@ -634,25 +635,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                     tc_fence_after();
                     const uint32_t tcol = tmem + lane_base + cur * 128 + wg * 64;
                     if (fp4) {
-                        // the unit's 64 code bytes and 8 scale bytes of this row, loaded first
-                        uint4 v[4];
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            v[q] = *reinterpret_cast<const uint4 *>(row + (((uu * 4 + q) ^ sw) << 4));
                         const uint2 sc = *reinterpret_cast<const uint2 *>(
                             raw + rs * kRawStageBytes + kRawScaleOff + wg * 2048 + r * 16 + uu * 8);
                         const uint32_t scw[2] = {sc.x, sc.y};
+                        const uint32_t row_s = sm100::smem_u32(row);
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {  // 16 B = 32 codes = 2 scale blocks
-                            const uint32_t vw[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
-                            const __half2 s2 = e4m3x2_to_half2(scw[q >> 1] >> (16 * (q & 1)));
+                            const uint32_t ca = row_s + (((uu * 4 + q) ^ sw) << 4);
+                            uint32_t hs0, hs1;  // the two block scales as f16, each in both halves
+                            e4m3x4_to_half2x2(scw[q >> 1] >> (16 * (q & 1)), hs0, hs1);
+                            const __half2 s2 = u32_h2(hs0);
                             const __half2 slo = __low2half2(s2), shi = __high2half2(s2);
                             uint32_t o[16];
 #pragma unroll
-                            for (int b = 0; b < 16; ++b) {
-                                // the conversion reads the low byte: no mask needed
-                                const __half2 h = e2m1x2_to_half2(vw[b >> 2] >> (8 * (b & 3)));
-                                o[b] = pack_h2(__hmul2(h, b < 8 ? slo : shi));
+                            for (int b = 0; b < 16; b += 4) {
+                                uint32_t h0, h1, h2, h3;
+                                e2m1x8_from_smem(ca + b, h0, h1, h2, h3);
+                                const __half2 sb = b < 8 ? slo : shi;
+                                o[b] = pack_h2(__hmul2(u32_h2(h0), sb));
+                                o[b + 1] = pack_h2(__hmul2(u32_h2(h1), sb));
+                                o[b + 2] = pack_h2(__hmul2(u32_h2(h2), sb));
+                                o[b + 3] = pack_h2(__hmul2(u32_h2(h3), sb));
                             }
                             tmem_st16(tcol + q * 16, o);
                         }
@@ -663,10 +666,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
 #pragma unroll
                             for (int hq = 0; hq < 2; ++hq) {
                                 const uint4 vv = *reinterpret_cast<const uint4 *>(row + (((q * 2 + hq) ^ sw) << 4));
-                                const uint32_t vw[4] = {vv.x, vv.y, vv.z, vv.w};
-#pragma unroll
-                                for (int b = 0; b < 8; ++b)
-                                    o[hq * 8 + b] = pack_h2(e4m3x2_to_half2(vw[b >> 1] >> (16 * (b & 1))));
+                                e4m3x4_to_half2x2(vv.x, o[hq * 8 + 0], o[hq * 8 + 1]);
+                                e4m3x4_to_half2x2(vv.y, o[hq * 8 + 2], o[hq * 8 + 3]);
+                                e4m3x4_to_half2x2(vv.z, o[hq * 8 + 4], o[hq * 8 + 5]);
+                                e4m3x4_to_half2x2(vv.w, o[hq * 8 + 6], o[hq * 8 + 7]);
                             }
                             tmem_st16(tcol + q * 16, o);
                         }
