@@ -55,8 +55,12 @@
 
 namespace moe {
 
-constexpr int kTcThreads = 832;
-constexpr int kDqWarps = 16;
+#ifndef MOE_TC_DQ_PARITIES
+#define MOE_TC_DQ_PARITIES 1
+#endif
+constexpr int kDqPar = MOE_TC_DQ_PARITIES;  // dequant warpgroups per tile (ping-pong when 2)
+constexpr int kDqWarps = 8 * kDqPar;
+constexpr int kTcThreads = 32 * (2 + 4 + kDqWarps + 4);
 constexpr int kTcMaxT = 64;
 constexpr int kNt = 32;               // columns per job at most (NVFP4, T > 16)
 constexpr int kNtSmall = 16;          // columns per job when T <= 16, and for FP8 jobs
@@ -154,9 +158,11 @@ struct TcSmem {
 };
 constexpr int kTcGroupArrays = 6;  // gu, dn, tile, mid, pair and x-column prefix sums
 
+// then two float arrays of C = T*(K+1): each (row, slot)'s combine weight and
+// down global scale (slot 0 = shared expert)
 __host__ __device__ inline int tc_smem_bytes(int T, int K) {
     const int C = T * (K + 1);
-    return TcSmem::tables + 4 * (group_table_ints(T, K) + kTcGroupArrays * (C + 1)) + 1024;
+    return TcSmem::tables + 4 * (group_table_ints(T, K) + kTcGroupArrays * (C + 1) + 2 * C) + 1024;
 }
 
 __device__ __forceinline__ uint32_t pack_h2(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
@@ -206,6 +212,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
     int *mid_prefix = tile_prefix + (C + 1);
     int *pair_prefix = mid_prefix + (C + 1);
     int *xcol_prefix = pair_prefix + (C + 1);
+    float *comb_w = reinterpret_cast<float *>(xcol_prefix + (C + 1));  // [T][K+1]
+    float *comb_g = comb_w + C;                                        // [T][K+1]
     uint32_t *err = &p.hdr->err;
 
     // ---- prologue: group table (scratch aliases the raw ring), per-group sums
@@ -331,6 +339,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
             }
         }
         if (range_bad) atomicOr(err, kErrRange);
+        // combine coefficients of every (row, slot): weight 1 and the shared
+        // down scale for slot 0, the router weight and the expert's down scale
+        // for pick slots
+        for (int i = tid; i < C; i += kTcThreads) {
+            const int t = i / (K + 1), q = i - t * (K + 1);
+            float w = 1.0f, gsc = 1.0f;
+            if (q == 0) {
+                if (p.shared.fmt == kFmtNvfp4) gsc = __ldg(p.shared.w2_gscale);
+            } else {
+                w = __ldg(p.topk_w + t * K + q - 1);
+                const int c = rcol[i];
+                if (c >= 0 && p.routed.fmt == kFmtNvfp4) gsc = __ldg(p.routed.w2_gscale + gexp[group_of_col(g0, G, c)]);
+            }
+            comb_w[i] = w;
+            comb_g[i] = gsc;
+        }
         __threadfence();
         __syncthreads();
         if (tid == 0)
@@ -593,7 +617,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
         // has its parity; it still steps through every unit and stage so its
         // ring positions stay in step with the others.
         const int dq = (warp - 6) >> 2;
-        const int wg = dq & 1, par = dq >> 1;
+        const int wg = dq & 1, par = dq >> 1;  // par < kDqPar
         const int r = ((warp & 3) << 5) | lane;  // row of the tile == TMEM lane
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         int js = 0, jph = 0, rs = 0, rph = 0, as = 0, aph = 0, ucount = 0;
@@ -626,7 +650,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                         as = 0;
                         aph ^= 1;
                     }
-                    if ((ucount & 1) != par) continue;
+                    if ((ucount % kDqPar) != par) continue;
                     const int cur_ph = (as == 0) ? (aph ^ 1) : aph;  // phase of slot `cur`
                     if (!__all_sync(0xffffffffu, mbar_wait(&sempty[cur], cur_ph ^ 1, abort_flag, err))) {
                         ok = false;
@@ -858,47 +882,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                     if (lane == 0) atom_add_acq_rel_gpu(p.group_ready + d.pair, 1u);
                 }
             } else {
-                // ---- down phase 2: the last job on a 256-row tile combines ----
+                // ---- down phase 2: count this (job, quarter) on its 256-row tile;
+                // the tile is combined once every down job has arrived ----
                 __threadfence();
                 __syncwarp();
-                int l = 0;
-                if (lane == 0)
-                    l = atom_add_acq_rel_gpu(p.htile_cnt + (size_t)d.tile * 4 + quarter, 1u) ==
-                        (uint32_t)dn_per_ht - 1;
-                if (__shfl_sync(0xffffffffu, l, 0)) {
-                    __threadfence();
-                    const int nkc_s = tc_nkc_dn(p.Is, T), nkc_r = tc_nkc_dn(p.I, T);
-                    const float gs_s = p.shared.fmt == kFmtNvfp4 ? __ldg(p.shared.w2_gscale) : 1.0f;
-                    for (int t = 0; t < T; ++t) {
-                        const int32_t *rc = rcol + t * (K + 1);
-#pragma unroll
-                        for (int hh = 0; hh < 2; ++hh) {
-                            const int h = hh ? h1 : h0;
-                            if (h >= H) continue;
-                            float acc = __bfloat162float(p.x[(size_t)t * H + h]);
-                            {
-                                const size_t col = (size_t)rc[0];
-                                float y = __ldcg(p.Y + col * H + h);
-                                for (int kc = 1; kc < nkc_s; ++kc)
-                                    y = __fadd_rn(y, __ldcg(p.Y + ((size_t)kc * p.Ucap + col) * H + h));
-                                acc = __fadd_rn(acc, __fmul_rn(y, gs_s));
-                            }
-                            for (int q = 0; q < K; ++q) {
-                                const int c = rc[1 + q];
-                                if (c < 0) continue;
-                                float y = __ldcg(p.Y + (size_t)c * H + h);
-                                for (int kc = 1; kc < nkc_r; ++kc)
-                                    y = __fadd_rn(y, __ldcg(p.Y + ((size_t)kc * p.Ucap + c) * H + h));
-                                const float gs = p.routed.fmt == kFmtNvfp4
-                                                     ? __ldg(p.routed.w2_gscale + p.ids[t * K + q])
-                                                     : 1.0f;
-                                acc = __fmaf_rn(p.topk_w[t * K + q], __fmul_rn(y, gs), acc);
-                            }
-                            p.out[(size_t)t * H + h] = __float2bfloat16_rn(acc);
-                        }
-                    }
-                    if (lane == 0) p.htile_cnt[(size_t)d.tile * 4 + quarter] = 0;
-                }
+                if (lane == 0) atom_add_acq_rel_gpu(p.htile_cnt + d.tile, 1u);
             }
         }
     }
@@ -910,6 +898,80 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
+
+    // ---- combine: every warp of the grid shares the output ------------------
+    // A warp unit is 32 consecutive outputs of one row. Once all 4*dn_per_ht
+    // (down job, quarter) arrivals of its 256-row tile are in, each lane sums
+    // its output in the fixed order x + y_shared*gs + sum over picks of
+    // w*(y*gs), each y the sum of its K-chunk partials in chunk order. The
+    // partials are loaded 16 at a time with no dependence between them, so a
+    // unit costs about one memory round trip per 16 terms.
+    if (!*abort_flag) {
+        const int nwarps = kTcThreads / 32, hw = H / 32;
+        const long long nwu = (long long)T * hw;
+        const uint32_t target = 4u * (uint32_t)dn_per_ht;
+        const int nkc_s = tc_nkc_dn(p.Is, T), nkc_r = tc_nkc_dn(p.I, T);
+        const int nterm = nkc_s + K * nkc_r;
+        unsigned long long seen = 0;  // 256-row tiles < 64 already seen complete
+        for (long long wu = (long long)blockIdx.x * nwarps + warp; wu < nwu; wu += (long long)gridDim.x * nwarps) {
+            const int t = (int)(wu / hw), h = (int)(wu % hw) * 32 + lane, ht = h >> 8;
+            if (!(ht < 64 && ((seen >> ht) & 1ull))) {
+                bool ready = ld_acquire_gpu(p.htile_cnt + ht) >= target;
+                if (!ready) {
+                    const unsigned long long t0 = globaltimer_ns();
+                    while (!(ready = ld_acquire_gpu(p.htile_cnt + ht) >= target)) {
+                        if ((*reinterpret_cast<volatile uint32_t *>(err) & kErrWaitTimeout) ||
+                            globaltimer_ns() - t0 > kWaitBudgetNs)
+                            break;
+                        __nanosleep(64);
+                    }
+                }
+                if (!__all_sync(0xffffffffu, ready)) {
+                    atomicOr(err, kErrWaitTimeout);
+                    break;
+                }
+                if (ht < 64) seen |= 1ull << ht;
+            }
+            const int32_t *rc = rcol + t * (K + 1);
+            const float *cw = comb_w + t * (K + 1), *cg = comb_g + t * (K + 1);
+            float acc = __bfloat162float(p.x[(size_t)t * H + h]);
+            float y = 0.0f;
+            int lq = 0, lk = 0;  // (slot, chunk) of the next term to load
+            int aq = 0, ak = 0;  // ... and to add
+            for (int b0 = 0; b0 < nterm; b0 += 16) {
+                float v[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    v[u] = 0.0f;
+                    if (b0 + u < nterm) {
+                        const int c = rc[lq];
+                        if (c >= 0) v[u] = __ldcg(p.Y + ((size_t)lk * p.Ucap + c) * H + h);
+                        if (++lk == (lq == 0 ? nkc_s : nkc_r)) {
+                            lk = 0;
+                            ++lq;
+                        }
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    if (b0 + u < nterm) {
+                        const int nk = aq == 0 ? nkc_s : nkc_r;
+                        y = ak == 0 ? v[u] : __fadd_rn(y, v[u]);
+                        if (ak == nk - 1) {
+                            if (rc[aq] >= 0) acc = __fmaf_rn(cw[aq], __fmul_rn(y, cg[aq]), acc);
+                            ak = 0;
+                            ++aq;
+                        } else {
+                            ++ak;
+                        }
+                    }
+                }
+            }
+            p.out[(size_t)t * H + h] = __float2bfloat16_rn(acc);
+        }
+    }
+    __syncthreads();
+
     if (tid == 0) {
         __threadfence();
         if (atom_add_acq_rel_gpu(&p.hdr->exit_cnt, 1u) == gridDim.x - 1) {
@@ -918,6 +980,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                 p.group_ready[i] = 0;
                 p.x_ready[i] = 0;
             }
+            for (int i = 0; i < H / 256; ++i) p.htile_cnt[i] = 0;
             p.hdr->job_next = 0;
             __threadfence();
             p.hdr->exit_cnt = 0;
