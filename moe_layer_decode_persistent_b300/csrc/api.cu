@@ -158,12 +158,13 @@ moe::WeightsDev to_dev(const moe_weights *w) {
 }
 
 size_t table_smem_bytes(const moe_shape *s) {
-    return sizeof(int32_t) * (size_t)(moe::group_table_ints(s->T, s->K) + moe::group_table_scratch_ints(s->E));
+    return sizeof(int32_t) * (size_t)(moe::group_table_ints(s->T, s->K) + moe::group_table_scratch_ints(s->T, s->K, s->E));
 }
 
 struct DevInfo {
     int nsm = 0;
     int max_smem_optin = 0;
+    int tc_static_smem = 0;  // static shared memory of the tensor-core kernel
 };
 
 std::mutex g_mu;
@@ -181,6 +182,10 @@ moe_status dev_info(DevInfo *out) {
         if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
         e = cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
         if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(smem)");
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, moe::fused_tc_kernel);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncGetAttributes");
+        d.tc_static_smem = (int)fa.sharedSizeBytes;
         it = g_dev.emplace(dev, d).first;
     }
     *out = it->second;
@@ -400,7 +405,12 @@ moe_status launch_fused_tc(const moe::FusedParams &fp, const WsLayout &L, const 
     p.x_ready = reinterpret_cast<uint32_t *>(ws + L.tc_xready);
     p.Ucap = s->T * (s->K + 1);
     p.Imax = std::max(s->I, s->I_shared);
-    const size_t smem = (size_t)moe::tc_smem_bytes(s->T, s->K);
+    // the raw weight ring gets as many stages as shared memory holds
+    const int smem_limit = d.max_smem_optin - d.tc_static_smem;
+    int nR = moe::kRawStagesMax;
+    while (nR > 4 && moe::tc_smem_bytes(s->T, s->K, nR) > smem_limit) --nR;
+    p.nR = nR;
+    const size_t smem = (size_t)moe::tc_smem_bytes(s->T, s->K, nR);
     int occ = 0;
     if ((st = plan_occupancy(moe::fused_tc_kernel, moe::kTcThreads, smem, d, &occ)) != MOE_OK) return st;
     cudaLaunchConfig_t cfg = {};

@@ -65,13 +65,12 @@ constexpr int kTcMaxT = 64;
 constexpr int kNt = 32;               // columns per job at most (NVFP4, T > 16)
 constexpr int kNtSmall = 16;          // columns per job when T <= 16, and for FP8 jobs
 constexpr int kUnitK = 128;           // K elements of one TMEM A unit per tile
-constexpr int kRawStages = 4;
+constexpr int kRawStagesMax = 6;      // raw weight ring: as many stages as shared memory holds, 4..6
 constexpr int kRawTileBytes = 16384;  // 128 rows x 128 bytes
 constexpr int kRawScaleOff = 2 * kRawTileBytes;
 constexpr int kRawStageBytes = 2 * kRawTileBytes + 2 * 2048;  // + NVFP4 scales
-constexpr int kBStages = 4;
-constexpr int kBStageBytes = kNt * kUnitK * 2;  // f16 [32][128]
-constexpr int kASlotsMax = 3;         // TMEM A slots: 3 when jobs have 16 columns, else 2
+constexpr int kBUnitBytes = kNt * kUnitK * 2;  // one B buffer: [32][128] f16 at most
+constexpr int kASlotsMax = 3;         // TMEM A slots (each with its B buffer): 3 when jobs have 16 columns, else 2
 constexpr int kIssuers = 4;
 constexpr int kJobSlots = 4;
 constexpr int kTmemCols = 512;
@@ -87,6 +86,7 @@ constexpr int kKcNvfp4 = 1792;
 constexpr int kKcFp8 = 1024;
 constexpr int kKcDown = 1024;
 constexpr int kSplitMaxT = 16;
+constexpr int kCombBatch = 20;  // combine: partial sums loaded per batch (18 for DSv3 shapes at T <= 16)
 
 struct TcMaps {
     CUtensorMap r13, r13s, r2, r2s, s13, s13s, s2, s2s;
@@ -100,6 +100,7 @@ struct TcParams {
     WeightsDev routed, shared;
     __nv_bfloat16 *out;
     int T, H, I, Is, E, K;
+    int nR;  // raw weight ring stages (4..kRawStagesMax)
     unsigned flags;
     WsHeader *hdr;
     uint32_t *group_ready;  // per (group, column tile)
@@ -145,24 +146,31 @@ __device__ __forceinline__ uint32_t b_off(int n, int k) {
     return (uint32_t)(((n >> 3) * 16 + (k >> 3)) * 128 + (n & 7) * 16 + (k & 7) * 2);
 }
 
-// Shared-memory layout of the fused kernel (dynamic, 1024-aligned base).
+// Shared-memory layout of the fused kernel (dynamic, 1024-aligned base): B
+// buffers, job slots, barriers, small words, the group table with its per-group
+// arrays, and last the raw weight ring (1024-aligned, for the 128-byte swizzle).
 struct TcSmem {
-    static constexpr int raw = 0;
-    static constexpr int bbuf = raw + kRawStages * kRawStageBytes;
-    static constexpr int jobs = bbuf + kBStages * kBStageBytes;
+    static constexpr int bbuf = 0;
+    static constexpr int jobs = bbuf + kASlotsMax * kBUnitBytes;
     static constexpr int bars = jobs + kJobSlots * (int)sizeof(TcJob);
     // jfull, jempty, rfull, rempty, sfull, sempty, dfull, dempty, drain[4]
-    static constexpr int nbars = 2 * kJobSlots + 2 * kRawStages + 2 * kASlotsMax + 2 * 2 + kIssuers;
+    static constexpr int nbars = 2 * kJobSlots + 2 * kRawStagesMax + 2 * kASlotsMax + 2 * 2 + kIssuers;
     static constexpr int misc = bars + nbars * 8;  // tmem addr, abort, flags
-    static constexpr int tables = misc + 64;       // group table, then per-group arrays
+    static constexpr int tile_ready = misc + 64;   // per 256-row output tile: combine may start (64 max)
+    static constexpr int tables = tile_ready + 256;  // group table, then per-group arrays
 };
 constexpr int kTcGroupArrays = 6;  // gu, dn, tile, mid, pair and x-column prefix sums
 
 // then two float arrays of C = T*(K+1): each (row, slot)'s combine weight and
 // down global scale (slot 0 = shared expert)
-__host__ __device__ inline int tc_smem_bytes(int T, int K) {
+__host__ __device__ inline int tc_raw_offset(int T, int K) {
     const int C = T * (K + 1);
-    return TcSmem::tables + 4 * (group_table_ints(T, K) + kTcGroupArrays * (C + 1) + 2 * C) + 1024;
+    const int end = TcSmem::tables + 4 * (group_table_ints(T, K) + kTcGroupArrays * (C + 1) + 2 * C);
+    return (end + 1023) & ~1023;
+}
+// Dynamic shared memory for nR raw stages (+1024 to align the base).
+__host__ __device__ inline int tc_smem_bytes(int T, int K, int nR) {
+    return tc_raw_offset(T, K) + nR * kRawStageBytes + 1024;
 }
 
 __device__ __forceinline__ uint32_t pack_h2(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
@@ -179,6 +187,65 @@ __device__ __forceinline__ int group_of_col(const int32_t *g0, int G, int c) {
     return lo;
 }
 
+// This CTA's share of the activation columns (column c goes to CTA c mod grid)
+// -> f16 in the MMA B layout of its (group, column tile); each converted column
+// is then counted in x_ready. Whole CTA calls.
+__device__ __forceinline__ void tc_convert_x(const TcParams &p, const GroupTable &tab, const int *xcol_prefix,
+                                             const int *pair_prefix) {
+    const int ctid = threadIdx.x, nthr = blockDim.x;
+    const int T = p.T, H = p.H, G = tab.G(), U = tab.U();
+    const int32_t *gexp = tab.gexp(), *gn = tab.gncols(), *g0 = tab.gcol0();
+    const int32_t *crow = tab.col_row();
+    const int per_col = H / 8;  // 16-byte items of one column
+    const int b = (int)blockIdx.x, nb = (int)gridDim.x;
+    const int ncols = U > b ? (U - 1 - b) / nb + 1 : 0;
+    const int nitems = ncols * per_col;
+    uint32_t range_bad = 0;
+    for (int i0 = ctid; i0 < nitems; i0 += 4 * nthr) {
+        uint4 v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {  // the loads first, so they are in flight together
+            const int it = i0 + j * nthr;
+            v[j] = make_uint4(0u, 0u, 0u, 0u);
+            if (it < nitems) {
+                const int c = b + (it / per_col) * nb;
+                v[j] = __ldg(reinterpret_cast<const uint4 *>(p.x + (size_t)crow[c] * H) + it % per_col);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int it = i0 + j * nthr;
+            if (it >= nitems) break;
+            const int c = b + (it / per_col) * nb, k8i = it % per_col;
+            const int g = group_of_col(g0, G, c);
+            const int nt = tc_nt(gexp[g] < 0 ? p.shared.fmt : p.routed.fmt, T);
+            const int ct = (c - g0[g]) / nt, cl = (c - g0[g]) % nt;
+            const int n = min(nt, gn[g] - ct * nt), npad = ((n + 15) / 16) * 16;
+            uint8_t *base = p.xB + ((long long)xcol_prefix[g] + (long long)ct * nt) * H * 2;
+            const uint32_t w4[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+            uint32_t o[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const __half2 h = __floats2half2_rn(bf16_bits_to_float(w4[k] & 0xffffu), bf16_bits_to_float(w4[k] >> 16));
+                if (__hisinf(__low2half(h)) || __hisinf(__high2half(h))) range_bad = 1;
+                o[k] = pack_h2(h);
+            }
+            *reinterpret_cast<uint4 *>(base + (long long)(k8i >> 4) * npad * 256 + b_off(cl, (k8i & 15) * 8)) =
+                make_uint4(o[0], o[1], o[2], o[3]);
+        }
+    }
+    if (range_bad) atomicOr(&p.hdr->err, kErrRange);
+    __threadfence();
+    __syncthreads();
+    if (ctid == 0)
+        for (int k = 0; k < ncols; ++k) {
+            const int c = b + k * nb;
+            const int g = group_of_col(g0, G, c);
+            const int nt = tc_nt(gexp[g] < 0 ? p.shared.fmt : p.routed.fmt, T);
+            red_add_release_gpu(p.x_ready + pair_prefix[g] + (c - g0[g]) / nt, 1u);
+        }
+}
+
 __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_constant__ TcParams p) {
     using namespace sm100;
     extern __shared__ __align__(1024) uint8_t smem_raw_[];
@@ -186,23 +253,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int T = p.T, K = p.K, H = p.H;
     const bool no_dedup = (p.flags & kFlagNoDedup) != 0;
-    const int nA = tc_aslots(T), ntmax = tc_ntmax(T);
+    const int nA = tc_aslots(T), ntmax = tc_ntmax(T), nR = p.nR;
     const int dcol0 = nA * 128, dset = 4 * ntmax;  // TMEM D set base and size
 
-    uint8_t *raw = smem + TcSmem::raw;
+    uint8_t *raw = smem + tc_raw_offset(T, K);
     uint8_t *bbuf = smem + TcSmem::bbuf;
     TcJob *jobs = reinterpret_cast<TcJob *>(smem + TcSmem::jobs);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + TcSmem::bars);
     uint64_t *jfull = bars, *jempty = jfull + kJobSlots;
-    uint64_t *rfull = jempty + kJobSlots, *rempty = rfull + kRawStages;
+    uint64_t *rfull = jempty + kJobSlots, *rempty = rfull + kRawStagesMax;
     // a unit slot = one TMEM A slot + one B buffer, filled by the dequant
     // warps and the B stager together and released by one commit per issuer
-    uint64_t *sfull = rempty + kRawStages, *sempty = sfull + kASlotsMax;
+    uint64_t *sfull = rempty + kRawStagesMax, *sempty = sfull + kASlotsMax;
     uint64_t *dfull = sempty + kASlotsMax, *dempty = dfull + 2;
     uint64_t *drain = dempty + 2;
     uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(smem + TcSmem::misc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + TcSmem::misc + 4);
     int *dn_per_ht_s = reinterpret_cast<int *>(smem + TcSmem::misc + 8);
+    uint32_t *tile_ready_s = reinterpret_cast<uint32_t *>(smem + TcSmem::tile_ready);
     int32_t *tbl = reinterpret_cast<int32_t *>(smem + TcSmem::tables);
     const int C = T * (K + 1);
     GroupTable tab{tbl, C};
@@ -276,7 +344,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                 mbar_init(&jfull[i], 1);
                 mbar_init(&jempty[i], 1 + kIssuers + kDqWarps + 4);  // stager, issuers, dequant, epilogue
             }
-            for (int i = 0; i < kRawStages; ++i) {
+            for (int i = 0; i < kRawStagesMax; ++i) {
                 mbar_init(&rfull[i], 1);
                 mbar_init(&rempty[i], kDqWarps);
             }
@@ -289,6 +357,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                 mbar_init(&dempty[i], 4);
             }
             for (int i = 0; i < kIssuers; ++i) mbar_init(&drain[i], 1);
+            for (int i = 0; i < 64; ++i) tile_ready_s[i] = 0;
             *abort_flag = 0;
             int dph_total = 0;  // down jobs that write one 256-row output tile
             for (int g = 0; g < G; ++g) {
@@ -301,6 +370,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
         }
     }
     if (warp == 1) tmem_alloc(tmem_base_s, kTmemCols);
+    if (warp >= 2) {
+        // combine coefficients of every (row, slot): weight 1 and the shared
+        // down scale for slot 0, the router weight and the expert's down scale
+        // for pick slots
+        for (int i = tid - 64; i < C; i += kTcThreads - 64) {
+            const int t = i / (K + 1), q = i - t * (K + 1);
+            float w = 1.0f, gsc = 1.0f;
+            if (q == 0) {
+                if (p.shared.fmt == kFmtNvfp4) gsc = __ldg(p.shared.w2_gscale);
+            } else {
+                w = __ldg(p.topk_w + t * K + q - 1);
+                const int c = rcol[i];
+                if (c >= 0 && p.routed.fmt == kFmtNvfp4)
+                    gsc = __ldg(p.routed.w2_gscale + gexp[group_of_col(g0, G, c)]);
+            }
+            comb_w[i] = w;
+            comb_g[i] = gsc;
+        }
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -309,62 +397,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
     const int njobs = NGU + NDN;
     const int dn_per_ht = *dn_per_ht_s;
 
-    // ---- this CTA's share of the activation columns -> f16 B tiles --------
-    // Column c goes to CTA c mod grid; every 128-K unit of its x row is
-    // converted once into the (group, column tile)'s B layout in global memory.
-    {
-        const int U = tab.U();
-        uint32_t range_bad = 0;
-        for (int c = blockIdx.x; c < U; c += gridDim.x) {
-            const int g = group_of_col(g0, G, c);
-            const int nt = tc_nt(gexp[g] < 0 ? p.shared.fmt : p.routed.fmt, T);
-            const int ct = (c - g0[g]) / nt, cl = (c - g0[g]) % nt;
-            const int n = min(nt, gn[g] - ct * nt), npad = ((n + 15) / 16) * 16;
-            uint8_t *base = p.xB + ((long long)xcol_prefix[g] + (long long)ct * nt) * H * 2;
-            const __nv_bfloat16 *xr = p.x + (size_t)crow[c] * H;
-            for (int it = tid; it < H / 8; it += kTcThreads) {
-                const int ku = it >> 4, k8 = it & 15;
-                const uint4 q = __ldg(reinterpret_cast<const uint4 *>(xr + it * 8));
-                const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
-                uint32_t o[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const __half2 h = __floats2half2_rn(bf16_bits_to_float(w4[k] & 0xffffu),
-                                                        bf16_bits_to_float(w4[k] >> 16));
-                    if (__hisinf(__low2half(h)) || __hisinf(__high2half(h))) range_bad = 1;
-                    o[k] = pack_h2(h);
-                }
-                *reinterpret_cast<uint4 *>(base + (long long)ku * npad * 256 + b_off(cl, k8 * 8)) =
-                    make_uint4(o[0], o[1], o[2], o[3]);
-            }
-        }
-        if (range_bad) atomicOr(err, kErrRange);
-        // combine coefficients of every (row, slot): weight 1 and the shared
-        // down scale for slot 0, the router weight and the expert's down scale
-        // for pick slots
-        for (int i = tid; i < C; i += kTcThreads) {
-            const int t = i / (K + 1), q = i - t * (K + 1);
-            float w = 1.0f, gsc = 1.0f;
-            if (q == 0) {
-                if (p.shared.fmt == kFmtNvfp4) gsc = __ldg(p.shared.w2_gscale);
-            } else {
-                w = __ldg(p.topk_w + t * K + q - 1);
-                const int c = rcol[i];
-                if (c >= 0 && p.routed.fmt == kFmtNvfp4) gsc = __ldg(p.routed.w2_gscale + gexp[group_of_col(g0, G, c)]);
-            }
-            comb_w[i] = w;
-            comb_g[i] = gsc;
-        }
-        __threadfence();
-        __syncthreads();
-        if (tid == 0)
-            for (int c = blockIdx.x; c < U; c += gridDim.x) {
-                const int g = group_of_col(g0, G, c);
-                const int nt = tc_nt(gexp[g] < 0 ? p.shared.fmt : p.routed.fmt, T);
-                atom_add_acq_rel_gpu(p.x_ready + pair_prefix[g] + (c - g0[g]) / nt, 1u);
-            }
-    }
-
+    tc_convert_x(p, tab, xcol_prefix, pair_prefix);
     auto job_at = [&](int slot) -> TcJob { return jobs[slot]; };
 
     if (warp == 0) {
@@ -473,7 +506,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                                          &rfull[rs], pol);
                     }
                     armed |= 1u << rs;
-                    if (++rs == kRawStages) {
+                    if (++rs == nR) {
                         rs = 0;
                         rph ^= 1;
                     }
@@ -482,7 +515,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
             }
             // never leave with a TMA write into shared memory still in flight
             if (*abort_flag && armed) {
-                for (int s = 0; s < kRawStages; ++s) {
+                for (int s = 0; s < nR; ++s) {
                     if (!(armed >> s & 1u)) continue;
                     // the phase armed last for slot s has parity rph if s < rs, else rph ^ 1
                     const uint32_t par = (s < rs) ? (uint32_t)rph : (uint32_t)(rph ^ 1);
@@ -495,6 +528,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
     } else if (warp == 1) {
         // ===================== B stager =====================
         int js = 0, jph = 0, bs = 0, bph = 0;  // unit slot ring position
+        const uint32_t bunit = (uint32_t)ntmax * kUnitK * 2;  // bytes of one B buffer
         for (;;) {
             if (!__all_sync(0xffffffffu, mbar_wait(&jfull[js], jph, abort_flag, err))) break;
             const TcJob d = job_at(js);
@@ -542,7 +576,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                 {
                     const int ku = d.k0 / kUnitK + u;  // global K unit index
                     const uint8_t *src = src0 + (long long)ku * bytes;
-                    uint8_t *dst = bbuf + bs * kBStageBytes;
+                    uint8_t *dst = bbuf + bs * bunit;
                     for (uint32_t o = (uint32_t)lane * 16; o < bytes; o += 32 * 16) cp_async16(dst + o, src + o);
                     cp_async_arrive_noinc(&sfull[bs]);
                 }
@@ -558,6 +592,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
         if (lane == 0) {
             const int q = warp - 2, tile = q & 1, kh = q >> 1;
             int js = 0, jph = 0, as = 0, aph = 0, ds = 0, dph = 0;
+            const uint32_t bunit = (uint32_t)ntmax * kUnitK * 2;
             bool issued = false;
             for (;;) {
                 if (!mbar_wait(&jfull[js], jph, abort_flag, err)) break;
@@ -580,7 +615,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                     tc_fence_after();
                     const uint32_t a = tmem + as * 128 + tile * 64;
                     const uint32_t dd = tmem + dcol0 + ds * dset + (tile * 2 + kh) * ntmax;
-                    const uint32_t bb = smem_u32(bbuf + as * kBStageBytes);
+                    const uint32_t bb = smem_u32(bbuf + as * bunit);
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const int ks = kh * 4 + k;
@@ -644,6 +679,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                 }
                 const uint8_t *row = raw + rs * kRawStageBytes + wg * kRawTileBytes + r * 128;
                 const int sw = r & 7;
+                // With three or more A slots a warp converts all of its units of
+                // the stage, then waits once for its TMEM stores and publishes them
+                // together; with two, each unit is published as soon as it is stored
+                // (the next unit's slot is the one the MMA is still reading).
+                const bool batch = nA >= 3;
+                int pend[2], npend = 0;
                 for (int uu = 0; uu < upst; ++uu, ++ucount) {
                     const int cur = as;
                     if (++as == nA) {
@@ -698,17 +739,30 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                             tmem_st16(tcol + q * 16, o);
                         }
                     }
+                    if (batch) {
+                        pend[npend++] = cur;
+                    } else {
+                        tmem_wait_st();
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&sfull[cur]);
+                    }
+                }
+                if (!ok) break;
+                // the stage's shared memory has been read (its values are in the
+                // TMEM stores' registers): release it before waiting for the stores
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&rempty[rs]);
+                if (++rs == nR) {
+                    rs = 0;
+                    rph ^= 1;
+                }
+                if (npend) {
                     tmem_wait_st();
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&sfull[cur]);
-                }
-                if (!ok) break;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&rempty[rs]);
-                if (++rs == kRawStages) {
-                    rs = 0;
-                    rph ^= 1;
+                    if (lane == 0)
+                        for (int i = 0; i < npend; ++i) mbar_arrive(&sfull[pend[i]]);
                 }
             }
             if (!ok) break;
@@ -891,46 +945,71 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
         }
     }
 
-    // ---- teardown -----------------------------------------------------------
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
-        tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
-    }
+    // A warp whose role's loop ran on lane 0 alone reconverges here.
+    __syncwarp();
 
     // ---- combine: every warp of the grid shares the output ------------------
-    // A warp unit is 32 consecutive outputs of one row. Once all 4*dn_per_ht
-    // (down job, quarter) arrivals of its 256-row tile are in, each lane sums
-    // its output in the fixed order x + y_shared*gs + sum over picks of
-    // w*(y*gs), each y the sum of its K-chunk partials in chunk order. The
-    // partials are loaded 16 at a time with no dependence between them, so a
-    // unit costs about one memory round trip per 16 terms.
-    if (!*abort_flag) {
-        const int nwarps = kTcThreads / 32, hw = H / 32;
+    // A 256-row output tile is complete once all 4*dn_per_ht (down job,
+    // quarter) arrivals are in. Warp 0 (the producer, which finishes first)
+    // watches every tile's counter with one load per lane per round and marks
+    // the complete ones in shared memory; the other warps start on the combine
+    // as soon as their role is done and wait on those marks, so the counters,
+    // which the epilogues are still incrementing, see one reader per CTA.
+    // A warp unit is 32 consecutive outputs of one row; units are dealt
+    // round-robin over the CTAs first and then over warps 1.. of a CTA in role
+    // order, so the warps that finish first take them first. Each lane sums its
+    // output in the fixed order x + y_shared*gs + sum over picks of w*(y*gs),
+    // each y the sum of its K-chunk partials in chunk order. The partials are
+    // loaded kCombBatch at a time with no dependence between them, so a unit
+    // costs about one memory round trip.
+    const uint32_t tile_target = 4u * (uint32_t)dn_per_ht;
+    if (warp == 0) {
+        const int nht = H / 256;  // <= 64
+        uint32_t pending = (lane < nht ? 1u : 0u) | (lane + 32 < nht ? 2u : 0u);
+        const unsigned long long t0 = globaltimer_ns();
+        unsigned nap = 128;
+        while (!*abort_flag) {
+#pragma unroll
+            for (int k = 0; k < 2; ++k)
+                if ((pending >> k) & 1u) {
+                    const int ht = lane + 32 * k;
+                    if (ld_acquire_gpu(p.htile_cnt + ht) >= tile_target) {
+                        st_release_cta_shared(tile_ready_s + ht, 1u);
+                        pending &= ~(1u << k);
+                    }
+                }
+            if (!__any_sync(0xffffffffu, pending != 0u)) break;
+            if ((*reinterpret_cast<volatile uint32_t *>(err) & kErrWaitTimeout) ||
+                globaltimer_ns() - t0 > kWaitBudgetNs) {
+                if (lane == 0) {
+                    atomicOr(err, kErrWaitTimeout);
+                    *abort_flag = 1;
+                }
+                break;
+            }
+            __nanosleep(nap);
+            if (nap < 512) nap <<= 1;
+        }
+        __syncwarp();
+    } else if (!*abort_flag) {
+        const int ncw = kTcThreads / 32 - 1, hw = H / 32;  // combine warps 1..
         const long long nwu = (long long)T * hw;
-        const uint32_t target = 4u * (uint32_t)dn_per_ht;
         const int nkc_s = tc_nkc_dn(p.Is, T), nkc_r = tc_nkc_dn(p.I, T);
         const int nterm = nkc_s + K * nkc_r;
-        unsigned long long seen = 0;  // 256-row tiles < 64 already seen complete
-        for (long long wu = (long long)blockIdx.x * nwarps + warp; wu < nwu; wu += (long long)gridDim.x * nwarps) {
+        for (long long wu = (long long)(warp - 1) * gridDim.x + blockIdx.x; wu < nwu;
+             wu += (long long)gridDim.x * ncw) {
             const int t = (int)(wu / hw), h = (int)(wu % hw) * 32 + lane, ht = h >> 8;
-            if (!(ht < 64 && ((seen >> ht) & 1ull))) {
-                bool ready = ld_acquire_gpu(p.htile_cnt + ht) >= target;
-                if (!ready) {
-                    const unsigned long long t0 = globaltimer_ns();
-                    while (!(ready = ld_acquire_gpu(p.htile_cnt + ht) >= target)) {
-                        if ((*reinterpret_cast<volatile uint32_t *>(err) & kErrWaitTimeout) ||
-                            globaltimer_ns() - t0 > kWaitBudgetNs)
-                            break;
-                        __nanosleep(64);
-                    }
+            if (!ld_acquire_cta_shared(tile_ready_s + ht)) {
+                const unsigned long long t0 = globaltimer_ns();
+                bool ready = false;
+                while (!(ready = ld_acquire_cta_shared(tile_ready_s + ht) != 0u)) {
+                    if (*abort_flag || globaltimer_ns() - t0 > kWaitBudgetNs) break;
+                    __nanosleep(64);
                 }
                 if (!__all_sync(0xffffffffu, ready)) {
                     atomicOr(err, kErrWaitTimeout);
                     break;
                 }
-                if (ht < 64) seen |= 1ull << ht;
             }
             const int32_t *rc = rcol + t * (K + 1);
             const float *cw = comb_w + t * (K + 1), *cg = comb_g + t * (K + 1);
@@ -938,10 +1017,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
             float y = 0.0f;
             int lq = 0, lk = 0;  // (slot, chunk) of the next term to load
             int aq = 0, ak = 0;  // ... and to add
-            for (int b0 = 0; b0 < nterm; b0 += 16) {
-                float v[16];
+            for (int b0 = 0; b0 < nterm; b0 += kCombBatch) {
+                float v[kCombBatch];
 #pragma unroll
-                for (int u = 0; u < 16; ++u) {
+                for (int u = 0; u < kCombBatch; ++u) {
                     v[u] = 0.0f;
                     if (b0 + u < nterm) {
                         const int c = rc[lq];
@@ -953,7 +1032,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                     }
                 }
 #pragma unroll
-                for (int u = 0; u < 16; ++u) {
+                for (int u = 0; u < kCombBatch; ++u) {
                     if (b0 + u < nterm) {
                         const int nk = aq == 0 ? nkc_s : nkc_r;
                         y = ak == 0 ? v[u] : __fadd_rn(y, v[u]);
@@ -970,8 +1049,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
             p.out[(size_t)t * H + h] = __float2bfloat16_rn(acc);
         }
     }
-    __syncthreads();
+    __syncwarp();
 
+    // ---- teardown -----------------------------------------------------------
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
     if (tid == 0) {
         __threadfence();
         if (atom_add_acq_rel_gpu(&p.hdr->exit_cnt, 1u) == gridDim.x - 1) {

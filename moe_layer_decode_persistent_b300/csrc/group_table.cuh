@@ -37,12 +37,12 @@ struct GroupTable {
 
 __host__ __device__ constexpr int group_table_ints(int T, int K) { return 2 + 5 * T * (K + 1); }
 
-// Shared-memory bytes group_table_cta needs besides the table: three per-expert
-// arrays of E ints.
-__host__ __device__ constexpr int group_table_scratch_ints(int E) { return 3 * E; }
+// Shared-memory ints group_table_cta needs besides the table: three per-expert
+// arrays of E ints and a copy of the T*K picks.
+__host__ __device__ constexpr int group_table_scratch_ints(int T, int K, int E) { return 3 * E + T * K; }
 
 // Build the table for ids [T][K] into `tab` (shared memory) using `scr`
-// (shared, group_table_scratch_ints(E) ints). Whole CTA calls; ends with a
+// (shared, group_table_scratch_ints(T, K, E) ints). Whole CTA calls; ends with a
 // __syncthreads. Error bits are OR-ed into *err_word when err_word != null.
 __device__ void group_table_cta(const int32_t *__restrict__ ids, int T, int K, int E,
                                 bool no_dedup, GroupTable tab, int *scr, uint32_t *err_word) {
@@ -50,6 +50,7 @@ __device__ void group_table_cta(const int32_t *__restrict__ ids, int T, int K, i
     const int tid = threadIdx.x, nthr = blockDim.x;
     const int lane = tid & 31, warp = tid >> 5;
     int *e_first = scr, *e_group = scr + E, *e_count = scr + 2 * E;
+    int *sid = scr + 3 * E;  // the picks, read from global memory once
     int32_t *gexp = tab.gexp(), *gn = tab.gncols(), *g0 = tab.gcol0(), *crow = tab.col_row(),
             *rcol = tab.row_col();
 
@@ -58,18 +59,19 @@ __device__ void group_table_cta(const int32_t *__restrict__ ids, int T, int K, i
         e_first[e] = INT_MAX;
         e_count[e] = 0;
     }
+    for (int j = tid; j < n; j += nthr) sid[j] = ids[j];
     __syncthreads();
 
     uint32_t err = 0;
     for (int j = tid; j < n; j += nthr) {
-        const int id = ids[j], t = j / K, p = j - t * K;
+        const int id = sid[j], t = j / K, p = j - t * K;
         if (id < 0 || id >= E) {
             err |= kErrBadExpert;
             continue;
         }
         atomicMin(&e_first[id], j);
         for (int q = 0; q < p; ++q)
-            if (ids[t * K + q] == id) err |= kErrDupExpert;
+            if (sid[t * K + q] == id) err |= kErrDupExpert;
     }
     if (err && err_word) atomicOr(err_word, err);
     __syncthreads();
@@ -88,7 +90,7 @@ __device__ void group_table_cta(const int32_t *__restrict__ ids, int T, int K, i
                     if (slot == 0) {
                         v = true;
                     } else {
-                        id = ids[t * K + slot - 1];
+                        id = sid[t * K + slot - 1];
                         v = id >= 0 && id < E;
                     }
                 }
@@ -118,7 +120,7 @@ __device__ void group_table_cta(const int32_t *__restrict__ ids, int T, int K, i
             }
             for (int base = 0; base < n; base += 32) {
                 const int j = base + lane;
-                const int id = j < n ? ids[j] : -1;
+                const int id = j < n ? sid[j] : -1;
                 const bool valid = j < n && id >= 0 && id < E;
                 const bool first = valid && e_first[id] == j;
                 const unsigned b = __ballot_sync(0xffffffffu, first);
@@ -173,7 +175,7 @@ __device__ void group_table_cta(const int32_t *__restrict__ ids, int T, int K, i
             crow[t] = t;
         }
         for (int j = tid; j < n; j += nthr) {
-            const int id = ids[j], t = j / K, p = j - t * K;
+            const int id = sid[j], t = j / K, p = j - t * K;
             if (id < 0 || id >= E) continue;
             const int c = g0[e_group[id]] + rcol[t * K1 + 1 + p];
             rcol[t * K1 + 1 + p] = c;

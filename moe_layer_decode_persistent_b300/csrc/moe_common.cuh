@@ -73,6 +73,24 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t *p, uint32_t v
     return old;
 }
 
+__device__ __forceinline__ void st_release_cta_shared(uint32_t *p, uint32_t v) {
+    asm volatile("st.release.cta.shared.u32 [%0], %1;" ::"r"((uint32_t)__cvta_generic_to_shared(p)), "r"(v)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_cta_shared(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.cta.shared.u32 %0, [%1];"
+                 : "=r"(v)
+                 : "r"((uint32_t)__cvta_generic_to_shared(p))
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void red_add_release_gpu(uint32_t *p, uint32_t v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 // 16 bytes of streamed (read-once) weights: skip L1.
 __device__ __forceinline__ uint4 ld_stream_v4(const void *p) {
     uint4 v;
