@@ -2,7 +2,7 @@
 HBM GB/s against the byte roofline, one JSON line on stdout.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload dsv3_t1|dsv3_t8|dsv3_t64] [--sweep]
+                  [--workload dsv3_t1|dsv3_t8|dsv3_t64] [--sweep] [--sweep-wide]
 
 A step is one launch of the whole layer (group table, gate/up + SwiGLU,
 down, router weights, shared expert, residual, bf16 write) over one batch.
@@ -10,8 +10,12 @@ The default workload is the DeepSeek-V3-shaped decode layer at T=1 (H=7168,
 routed I=2048 NVFP4 E=256 top-8, shared I=2048 FP8 128x128 blocks, uniform
 routing). Four copies of the layer's weights are resident and the steps
 rotate over them, so each step reads weights that are not in L2 (126 MB).
---impl reference times the fp64 CPU oracle on a bounded sample of the same
-workload (the reference arm). Under torchrun every rank runs its own replica
+Every timing is also taken with the launches captured in a CUDA graph and
+replayed (`graph_us_per_launch`). --sweep adds the T=8 and T=64 workloads;
+--sweep-wide the wide-expert layer (E=384 top-8, uniform routing) at
+T = 1, 2, 4, ..., 256 with 4 distinct layers' weights resident, run back to
+back. --impl reference times the fp64 CPU oracle on a bounded sample of the
+same workload (the reference arm). Under torchrun every rank runs its own replica
 (the build has no cross-GPU exchange); rank 0 prints the max over ranks.
 """
 from __future__ import annotations
@@ -226,7 +230,7 @@ def run_ours(args, rank, world, local):
     if args.no_e2e:
         return dict(us_launch=us_launch_max, ms_per_step=ms_per_step, algo_bytes=algo_bytes,
                     distinct=distinct, clocks=clk.summary(), err=err, e2e_us=None, h2d=0, d2h=0,
-                    sweep={}, T=shape.T)
+                    sweep={}, wide={}, graph_us=None, T=shape.T)
     xh = L.x.cpu().pin_memory()
     ih = L.topk_ids.cpu().pin_memory()
     wh = L.topk_w.cpu().pin_memory()
@@ -246,16 +250,51 @@ def run_ours(args, rank, world, local):
     e2e_us = max_over_ranks(e2e_us, world, dev)
     assert torch.equal(oh.view(torch.int16), out.cpu().view(torch.int16))
 
+    def launch_s(i, s):
+        rw, sw = weights[i % len(weights)]
+        B.moe_fused_decode(L.x, L.topk_ids, L.topk_w, rw, sw, out, sh, ws, stream=s)
+
+    graph_us = graph_us_per_launch(launch_s, 4 * len(weights))
+    assert B.moe_read_error(ws) == 0
+
     sweep = {}
     if args.sweep:
         for name in WORKLOADS:
             if name == args.workload:
                 continue
             sweep[name] = sweep_point(name, args, dev)
+    wide = wide_sweep(args, dev) if args.sweep_wide else {}
     return dict(us_launch=us_launch_max, ms_per_step=ms_per_step, algo_bytes=algo_bytes,
                 distinct=distinct, clocks=clk.summary(), err=err, e2e_us=e2e_us,
                 h2d=xh.numel() * 2 + ih.numel() * 4 + wh.numel() * 4, d2h=oh.numel() * 2,
-                sweep=sweep, T=shape.T)
+                sweep=sweep, wide=wide, graph_us=graph_us, T=shape.T)
+
+
+def graph_us_per_launch(launch, n_launch: int, reps: int = 5) -> float:
+    """us per launch with `n_launch` launches captured in one CUDA graph and the
+    graph replayed `reps` times (events on the capturing stream)."""
+    import torch
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        launch(0, s)  # warm (outside capture)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            for i in range(n_launch):
+                launch(i, s)
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        a.record(s)
+        for _ in range(reps):
+            g.replay()
+        b.record(s)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) * 1e3 / (reps * n_launch)
 
 
 def sweep_point(name, args, dev):
@@ -288,13 +327,80 @@ def sweep_point(name, args, dev):
     torch.cuda.synchronize()
     assert B.moe_read_error(ws) == 0
     us = statistics.mean(a.elapsed_time(b) * 1e3 for a, b in ev)
+
+    def launch_s(i, s):
+        B.moe_fused_decode(L.x, L.topk_ids, L.topk_w, *weights[i % N_COPIES], out, sh, ws, stream=s)
+
+    g_us = graph_us_per_launch(launch_s, 2 * N_COPIES)
+    assert B.moe_read_error(ws) == 0
     b, distinct = algorithmic_bytes(L, L.topk_ids.cpu())
     peak, _ = measured_peaks()
     gbs = b / (us * 1e-6) / 1e9
     del L, copies, weights
     torch.cuda.empty_cache()
-    return {"us_per_launch": round(us, 2), "hbm_gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
-            "distinct_experts": distinct, "algo_bytes": b}
+    return {"us_per_launch": round(us, 2), "graph_us_per_launch": round(g_us, 2), "hbm_gbs": round(gbs, 1),
+            "frac": round(gbs / peak, 4), "distinct_experts": distinct, "algo_bytes": b}
+
+
+WIDE_T = [1, 2, 4, 8, 16, 32, 64, 128, 256]
+
+
+def wide_sweep(args, dev, n_layers: int = 4):
+    """Wide-expert layer (E=384 top-8, H=7168, I=2048, NVFP4 routed / FP8 shared,
+    uniform routing): us per launch at each T, launches over n_layers distinct
+    layers' resident weights run back to back."""
+    import torch
+
+    from moe_layer_decode_persistent_b300 import binding as B
+    from moe_layer_decode_persistent_b300 import inputs
+    E = 384
+    base = inputs.dsv3(1, E=E)
+    layers = []
+    for l in range(n_layers):
+        r = inputs.make_experts(inputs.FMT_NVFP4, E, base.H, base.I, ("L", l, 0), dev, tag="routed")
+        s_ = inputs.make_experts(inputs.FMT_FP8_B128, 1, base.H, base.I_shared, ("L", l, 0), dev, tag="shared")
+        layers.append((r, s_, B.make_weights(r), B.make_weights(s_)))
+    peak, _ = measured_peaks()
+    res = {}
+    for T in WIDE_T:
+        shape = inputs.dsv3(T, E=E)
+        ids = inputs.ROUTINGS["uniform"](T, shape.K, E, 0).to(dev)
+        w = inputs.router_weights(T, shape.K, 0).to(dev)
+        x = inputs.activations(T, shape.H, 0, dev)
+        sh = B.make_shape(T, shape.H, shape.I, shape.I_shared, E, shape.K, args.flags)
+        ws = torch.empty(B.moe_workspace_bytes(sh), dtype=torch.uint8, device=dev)
+        B.moe_workspace_init(ws)
+        out = torch.empty(T, shape.H, dtype=torch.bfloat16, device=dev)
+
+        def launch_s(i, s):
+            _, _, rw, sw = layers[i % n_layers]
+            B.moe_fused_decode(x, ids, w, rw, sw, out, sh, ws, stream=s)
+
+        stream = torch.cuda.current_stream(dev)
+        for i in range(2 * n_layers):
+            launch_s(i, stream)
+        n = 4 * n_layers
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for i in range(n):
+            launch_s(i, stream)
+        b.record(stream)
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) * 1e3 / n
+        g_us = graph_us_per_launch(launch_s, 2 * n_layers)
+        assert B.moe_read_error(ws) == 0
+        distinct = len(set(int(e) for e in ids.cpu().reshape(-1).tolist()))
+        byt = distinct * layers[0][0].nbytes_expert() + layers[0][1].nbytes_expert() + 4 * T * shape.H + 8 * T * shape.K
+        gbs = byt / (us * 1e-6) / 1e9
+        res[str(T)] = {"us_per_launch": round(us, 2), "graph_us_per_launch": round(g_us, 2),
+                       "hbm_gbs": round(gbs, 1), "frac": round(gbs / peak, 4), "distinct_experts": distinct,
+                       "algo_bytes": byt}
+        del ws, out
+    del layers
+    torch.cuda.empty_cache()
+    return res
 
 
 def oracle_sample(workload: str, n_experts_per_step: int = 1):
@@ -359,6 +465,8 @@ def main():
     ap.add_argument("--workload", choices=list(WORKLOADS), default="dsv3_t1")
     ap.add_argument("--flags", type=int, default=0)
     ap.add_argument("--sweep", action="store_true", help="also time the T=8 and T=64 workloads")
+    ap.add_argument("--sweep-wide", action="store_true",
+                    help="also time the wide-expert layer (E=384) at T=1..256, 4 layers back to back")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer (end-to-end) timing")
     ap.add_argument("--experts", type=int, default=256,
@@ -414,9 +522,12 @@ def main():
         {"value": round(r["e2e_us"], 2), "unit": "us", "h2d_bytes_per_step": r["h2d"],
          "d2h_bytes_per_step": r["d2h"]},
         "gpu_launches": args.steps, "clocks": r["clocks"], "device_error_word": r["err"],
+        "graph_us_per_launch": None if r["graph_us"] is None else round(r["graph_us"], 2),
     }
     if r["sweep"]:
         line["sweep"] = r["sweep"]
+    if r["wide"]:
+        line["wide_sweep"] = r["wide"]
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args)
     print(json.dumps(line), flush=True)

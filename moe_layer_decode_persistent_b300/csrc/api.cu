@@ -81,10 +81,14 @@ WsLayout ws_layout(const moe_shape *s) {
     off += nkc_gu * 2 * Ucap * Imax * sizeof(float);
     L.tc_Y = off = align_up(off, 256);
     off += (size_t)moe::tc_nkc_dn((int)Imax, Ti) * Ucap * H * sizeof(float);
+    // sum over (group, column tile) of the padded column counts: each group pads
+    // its last column tile to a multiple of 16, so it is at most U + 15 * G <=
+    // 16 * U in either form (the size does not depend on the flags)
+    const size_t cols_padded = 16 * Ucap;
     L.tc_midB = off = align_up(off, 256);
-    off += 16 * Ucap * (Imax / 128) * 256;  // sum of padded column counts <= 16 * Ucap
+    off += cols_padded * (Imax / 128) * 256;
     L.tc_xB = off = align_up(off, 256);
-    off += 16 * Ucap * H * 2;
+    off += cols_padded * H * 2;
     L.tc_end = align_up(off, 256);
 
     L.dev_total = off = std::max(L.fma_end, L.tc_end);
@@ -362,7 +366,17 @@ bool tc_eligible(const moe_shape *s, const moe_weights *routed, const moe_weight
         return false;
     }
     if (s->T > moe::kTcMaxT) {
-        *why = "T above 64";
+        *why = "T above 256";
+        return false;
+    }
+    DevInfo d;
+    if (dev_info(&d) != MOE_OK) {
+        *why = "device query failed";
+        return false;
+    }
+    const bool nd = (s->flags & MOE_FLAG_NO_DEDUP) != 0;
+    if (moe::tc_smem_bytes(s->T, s->K, s->E, nd, moe::kRawStagesMin) > d.max_smem_optin - d.tc_static_smem) {
+        *why = "group tables do not fit in shared memory";
         return false;
     }
     return true;
@@ -407,10 +421,11 @@ moe_status launch_fused_tc(const moe::FusedParams &fp, const WsLayout &L, const 
     p.Imax = std::max(s->I, s->I_shared);
     // the raw weight ring gets as many stages as shared memory holds
     const int smem_limit = d.max_smem_optin - d.tc_static_smem;
+    const bool nd = (s->flags & MOE_FLAG_NO_DEDUP) != 0;
     int nR = moe::kRawStagesMax;
-    while (nR > 4 && moe::tc_smem_bytes(s->T, s->K, nR) > smem_limit) --nR;
+    while (nR > moe::kRawStagesMin && moe::tc_smem_bytes(s->T, s->K, s->E, nd, nR) > smem_limit) --nR;
     p.nR = nR;
-    const size_t smem = (size_t)moe::tc_smem_bytes(s->T, s->K, nR);
+    const size_t smem = (size_t)moe::tc_smem_bytes(s->T, s->K, s->E, nd, nR);
     int occ = 0;
     if ((st = plan_occupancy(moe::fused_tc_kernel, moe::kTcThreads, smem, d, &occ)) != MOE_OK) return st;
     cudaLaunchConfig_t cfg = {};

@@ -208,7 +208,7 @@ __global__ void __launch_bounds__(kFmaThreads) fused_fma_kernel(FusedParams p) {
     int32_t *tbl = reinterpret_cast<int32_t *>(smem_i4);
     const int T = p.T, K = p.K, H = p.H;
     const bool no_dedup = (p.flags & kFlagNoDedup) != 0;
-    GroupTable tab{tbl, T * (K + 1)};
+    GroupTable tab{tbl, T * (K + 1), T * (K + 1)};
     int *scr = tbl + group_table_ints(T, K);
     group_table_cta(p.ids, T, K, p.E, no_dedup, tab, scr, blockIdx.x == 0 ? &p.hdr->err : nullptr);
 
@@ -305,7 +305,7 @@ __global__ void __launch_bounds__(256) group_table_kernel(const int32_t *ids, in
                                                           uint32_t *err_word) {
     extern __shared__ int4 smem_i4[];
     int32_t *tbl = reinterpret_cast<int32_t *>(smem_i4);
-    GroupTable tab{tbl, T * (K + 1)};
+    GroupTable tab{tbl, T * (K + 1), T * (K + 1)};
     int *scr = tbl + group_table_ints(T, K);
     group_table_cta(ids, T, K, E, (flags & kFlagNoDedup) != 0, tab, scr, err_word);
     for (int i = threadIdx.x; i < group_table_ints(T, K); i += blockDim.x) out[i] = tbl[i];

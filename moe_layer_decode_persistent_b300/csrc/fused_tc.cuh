@@ -61,11 +61,12 @@ namespace moe {
 constexpr int kDqPar = MOE_TC_DQ_PARITIES;  // dequant warpgroups per tile (ping-pong when 2)
 constexpr int kDqWarps = 8 * kDqPar;
 constexpr int kTcThreads = 32 * (2 + 4 + kDqWarps + 4);
-constexpr int kTcMaxT = 64;
+constexpr int kTcMaxT = 256;
 constexpr int kNt = 32;               // columns per job at most (NVFP4, T > 16)
 constexpr int kNtSmall = 16;          // columns per job when T <= 16, and for FP8 jobs
 constexpr int kUnitK = 128;           // K elements of one TMEM A unit per tile
-constexpr int kRawStagesMax = 6;      // raw weight ring: as many stages as shared memory holds, 4..6
+constexpr int kRawStagesMax = 6;      // raw weight ring: as many stages as shared memory holds, 2..6
+constexpr int kRawStagesMin = 2;
 constexpr int kRawTileBytes = 16384;  // 128 rows x 128 bytes
 constexpr int kRawScaleOff = 2 * kRawTileBytes;
 constexpr int kRawStageBytes = 2 * kRawTileBytes + 2 * 2048;  // + NVFP4 scales
@@ -100,7 +101,7 @@ struct TcParams {
     WeightsDev routed, shared;
     __nv_bfloat16 *out;
     int T, H, I, Is, E, K;
-    int nR;  // raw weight ring stages (4..kRawStagesMax)
+    int nR;  // raw weight ring stages (kRawStagesMin..kRawStagesMax)
     unsigned flags;
     WsHeader *hdr;
     uint32_t *group_ready;  // per (group, column tile)
@@ -161,16 +162,17 @@ struct TcSmem {
 };
 constexpr int kTcGroupArrays = 6;  // gu, dn, tile, mid, pair and x-column prefix sums
 
-// then two float arrays of C = T*(K+1): each (row, slot)'s combine weight and
-// down global scale (slot 0 = shared expert)
-__host__ __device__ inline int tc_raw_offset(int T, int K) {
-    const int C = T * (K + 1);
-    const int end = TcSmem::tables + 4 * (group_table_ints(T, K) + kTcGroupArrays * (C + 1) + 2 * C);
+// The group table (per-group arrays of capacity gcap), the per-group prefix
+// sums (gcap + 1 each), then two float arrays of C = T*(K+1): each (row, slot)'s
+// combine weight and down global scale (slot 0 = shared expert).
+__host__ __device__ inline int tc_raw_offset(int T, int K, int E, bool no_dedup) {
+    const int C = T * (K + 1), gcap = group_capacity(T, K, E, no_dedup);
+    const int end = TcSmem::tables + 4 * (group_table_ints_cap(T, K, gcap) + kTcGroupArrays * (gcap + 1) + 2 * C);
     return (end + 1023) & ~1023;
 }
 // Dynamic shared memory for nR raw stages (+1024 to align the base).
-__host__ __device__ inline int tc_smem_bytes(int T, int K, int nR) {
-    return tc_raw_offset(T, K) + nR * kRawStageBytes + 1024;
+__host__ __device__ inline int tc_smem_bytes(int T, int K, int E, bool no_dedup, int nR) {
+    return tc_raw_offset(T, K, E, no_dedup) + nR * kRawStageBytes + 1024;
 }
 
 __device__ __forceinline__ uint32_t pack_h2(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
@@ -256,7 +258,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
     const int nA = tc_aslots(T), ntmax = tc_ntmax(T), nR = p.nR;
     const int dcol0 = nA * 128, dset = 4 * ntmax;  // TMEM D set base and size
 
-    uint8_t *raw = smem + tc_raw_offset(T, K);
+    uint8_t *raw = smem + tc_raw_offset(T, K, p.E, no_dedup);
     uint8_t *bbuf = smem + TcSmem::bbuf;
     TcJob *jobs = reinterpret_cast<TcJob *>(smem + TcSmem::jobs);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + TcSmem::bars);
@@ -272,15 +274,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
     int *dn_per_ht_s = reinterpret_cast<int *>(smem + TcSmem::misc + 8);
     uint32_t *tile_ready_s = reinterpret_cast<uint32_t *>(smem + TcSmem::tile_ready);
     int32_t *tbl = reinterpret_cast<int32_t *>(smem + TcSmem::tables);
-    const int C = T * (K + 1);
-    GroupTable tab{tbl, C};
-    int *gu_prefix = tbl + group_table_ints(T, K);
-    int *dn_prefix = gu_prefix + (C + 1);
-    int *tile_prefix = dn_prefix + (C + 1);
-    int *mid_prefix = tile_prefix + (C + 1);
-    int *pair_prefix = mid_prefix + (C + 1);
-    int *xcol_prefix = pair_prefix + (C + 1);
-    float *comb_w = reinterpret_cast<float *>(xcol_prefix + (C + 1));  // [T][K+1]
+    const int C = T * (K + 1), gcap = group_capacity(T, K, p.E, no_dedup);
+    GroupTable tab{tbl, C, gcap};
+    int *gu_prefix = tbl + tab.ints();
+    int *dn_prefix = gu_prefix + (gcap + 1);
+    int *tile_prefix = dn_prefix + (gcap + 1);
+    int *mid_prefix = tile_prefix + (gcap + 1);
+    int *pair_prefix = mid_prefix + (gcap + 1);
+    int *xcol_prefix = pair_prefix + (gcap + 1);
+    float *comb_w = reinterpret_cast<float *>(xcol_prefix + (gcap + 1));  // [T][K+1]
     float *comb_g = comb_w + C;                                        // [T][K+1]
     uint32_t *err = &p.hdr->err;
 

@@ -21,21 +21,34 @@
 
 namespace moe {
 
-// Table layout (int32), C = T*(K+1): [0] G, [1] U, group_expert[C],
-// group_ncols[C], group_col0[C], col_row[C], row_col[T][K+1].
+// Table layout (int32), C = T*(K+1), gcap >= G the capacity of the per-group
+// arrays: [0] G, [1] U, group_expert[gcap], group_ncols[gcap], group_col0[gcap],
+// col_row[C], row_col[T][K+1]. The exported table (moe_group_table) has
+// gcap = C; the tensor-core kernel keeps it on chip with gcap = min(E, T*K) + 1
+// (dedup form) so large T still fits.
 struct GroupTable {
     int32_t *base;
     int C;
+    int gcap;
     __device__ __forceinline__ int32_t &G() const { return base[0]; }
     __device__ __forceinline__ int32_t &U() const { return base[1]; }
     __device__ __forceinline__ int32_t *gexp() const { return base + 2; }
-    __device__ __forceinline__ int32_t *gncols() const { return base + 2 + C; }
-    __device__ __forceinline__ int32_t *gcol0() const { return base + 2 + 2 * C; }
-    __device__ __forceinline__ int32_t *col_row() const { return base + 2 + 3 * C; }
-    __device__ __forceinline__ int32_t *row_col() const { return base + 2 + 4 * C; }
+    __device__ __forceinline__ int32_t *gncols() const { return base + 2 + gcap; }
+    __device__ __forceinline__ int32_t *gcol0() const { return base + 2 + 2 * gcap; }
+    __device__ __forceinline__ int32_t *col_row() const { return base + 2 + 3 * gcap; }
+    __device__ __forceinline__ int32_t *row_col() const { return base + 2 + 3 * gcap + C; }
+    __device__ __forceinline__ int ints() const { return 2 + 3 * gcap + 2 * C; }
 };
 
 __host__ __device__ constexpr int group_table_ints(int T, int K) { return 2 + 5 * T * (K + 1); }
+__host__ __device__ constexpr int group_table_ints_cap(int T, int K, int gcap) {
+    return 2 + 3 * gcap + 2 * T * (K + 1);
+}
+// Groups a launch can have: every (row, slot) use in the one-row form, else
+// the shared expert plus at most min(E, T*K) distinct routed experts.
+__host__ __device__ constexpr int group_capacity(int T, int K, int E, bool no_dedup) {
+    return no_dedup ? T * (K + 1) : 1 + (E < T * K ? E : T * K);
+}
 
 // Shared-memory ints group_table_cta needs besides the table: three per-expert
 // arrays of E ints and a copy of the T*K picks.
@@ -54,7 +67,7 @@ __device__ void group_table_cta(const int32_t *__restrict__ ids, int T, int K, i
     int32_t *gexp = tab.gexp(), *gn = tab.gncols(), *g0 = tab.gcol0(), *crow = tab.col_row(),
             *rcol = tab.row_col();
 
-    for (int i = tid; i < 2 + 5 * C; i += nthr) tab.base[i] = 0;
+    for (int i = tid; i < tab.ints(); i += nthr) tab.base[i] = 0;
     for (int e = tid; e < E; e += nthr) {
         e_first[e] = INT_MAX;
         e_count[e] = 0;

@@ -69,6 +69,40 @@ def test_dsv3_t64_zipf_sampled_rows(path):
 
 
 @pytest.mark.parametrize("path", list(PATHS))
+@pytest.mark.parametrize("T", [65, 200])
+def test_small_layers_beyond_64_rows(path, T):
+    """Above 64 rows the tensor path keeps its per-group tables at the group
+    capacity (shared + min(E, T*K) experts), not at T*(K+1)."""
+    s = inputs.Shape(T=T, H=SMALL.H, I=SMALL.I, I_shared=SMALL.I_shared, E=SMALL.E, K=SMALL.K)
+    L = layer(s, "zipf", seed=T, used_only=False)
+    out = run_fused(L, PATHS[path])
+    assert_parity(out, oracle_ref(L))
+    one_row = run_fused(L, PATHS[path] | B.MOE_FLAG_NO_DEDUP)
+    assert torch.equal(out.view(torch.int16), one_row.view(torch.int16))
+
+
+@pytest.fixture(scope="module")
+def wide_t256():
+    """Wide-expert layer: E=384 top-8, T=256 uniform rows (about 380 distinct)."""
+    return layer(inputs.dsv3(256, E=384), "uniform", seed=0)
+
+
+@pytest.mark.parametrize("path", ["mma", "auto"])
+def test_wide_expert_T256_sampled_rows(path, wide_t256):
+    L = wide_t256
+    rows = [0, 101, 255]
+    out = run_fused(L, PATHS[path])
+    assert_parity(out, oracle_ref(L, rows=rows), rows=rows)
+    assert torch.isfinite(out.float()).all()
+
+
+def test_wide_expert_T256_dedup_is_bitwise_equal_to_one_row_form(wide_t256):
+    a = run_fused(wide_t256, PATHS["mma"])
+    b = run_fused(wide_t256, PATHS["mma"] | B.MOE_FLAG_NO_DEDUP)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+@pytest.mark.parametrize("path", list(PATHS))
 @pytest.mark.parametrize("case", ["small_zipf_T13", "dsv3_T8_mtp", "dsv3_T64_zipf"])
 def test_dedup_is_bitwise_equal_to_one_row_form(path, case):
     if case == "small_zipf_T13":
