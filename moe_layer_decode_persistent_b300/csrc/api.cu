@@ -187,7 +187,7 @@ moe_status dev_info(DevInfo *out) {
         e = cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
         if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(smem)");
         cudaFuncAttributes fa;
-        e = cudaFuncGetAttributes(&fa, moe::fused_tc_kernel);
+        e = cudaFuncGetAttributes(&fa, moe::fused_tc_kernel<false>);
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncGetAttributes");
         d.tc_static_smem = (int)fa.sharedSizeBytes;
         it = g_dev.emplace(dev, d).first;
@@ -427,7 +427,9 @@ moe_status launch_fused_tc(const moe::FusedParams &fp, const WsLayout &L, const 
     p.nR = nR;
     const size_t smem = (size_t)moe::tc_smem_bytes(s->T, s->K, s->E, nd, nR);
     int occ = 0;
-    if ((st = plan_occupancy(moe::fused_tc_kernel, moe::kTcThreads, smem, d, &occ)) != MOE_OK) return st;
+    const bool capped = moe::tc_capped_tables(s->T);
+    auto kern = capped ? moe::fused_tc_kernel<true> : moe::fused_tc_kernel<false>;
+    if ((st = plan_occupancy(kern, moe::kTcThreads, smem, d, &occ)) != MOE_OK) return st;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)d.nsm);  // one CTA per SM: it holds all of TMEM
     cfg.blockDim = dim3(moe::kTcThreads);
@@ -438,7 +440,7 @@ moe_status launch_fused_tc(const moe::FusedParams &fp, const WsLayout &L, const 
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, moe::fused_tc_kernel, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
     if (e != cudaSuccess) return cuda_fail(e, "launch fused_tc_kernel");
     return MOE_OK;
 }

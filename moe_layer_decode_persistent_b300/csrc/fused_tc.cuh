@@ -164,15 +164,22 @@ constexpr int kTcGroupArrays = 6;  // gu, dn, tile, mid, pair and x-column prefi
 
 // The group table (per-group arrays of capacity gcap), the per-group prefix
 // sums (gcap + 1 each), then two float arrays of C = T*(K+1): each (row, slot)'s
-// combine weight and down global scale (slot 0 = shared expert).
-__host__ __device__ inline int tc_raw_offset(int T, int K, int E, bool no_dedup) {
-    const int C = T * (K + 1), gcap = group_capacity(T, K, E, no_dedup);
+// combine weight and down global scale (slot 0 = shared expert). Up to
+// kTcFullTablesMaxT rows the per-group arrays hold C entries (the compiler then
+// sees a fixed layout); above, they hold the group capacity so the tables fit.
+constexpr int kTcFullTablesMaxT = 64;
+__host__ __device__ inline bool tc_capped_tables(int T) { return T > kTcFullTablesMaxT; }
+__host__ __device__ inline int tc_gcap(int T, int K, int E, bool no_dedup) {
+    return tc_capped_tables(T) ? group_capacity(T, K, E, no_dedup) : T * (K + 1);
+}
+__host__ __device__ inline int tc_raw_offset(int T, int K, int gcap) {
+    const int C = T * (K + 1);
     const int end = TcSmem::tables + 4 * (group_table_ints_cap(T, K, gcap) + kTcGroupArrays * (gcap + 1) + 2 * C);
     return (end + 1023) & ~1023;
 }
 // Dynamic shared memory for nR raw stages (+1024 to align the base).
 __host__ __device__ inline int tc_smem_bytes(int T, int K, int E, bool no_dedup, int nR) {
-    return tc_raw_offset(T, K, E, no_dedup) + nR * kRawStageBytes + 1024;
+    return tc_raw_offset(T, K, tc_gcap(T, K, E, no_dedup)) + nR * kRawStageBytes + 1024;
 }
 
 __device__ __forceinline__ uint32_t pack_h2(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
@@ -248,6 +255,7 @@ __device__ __forceinline__ void tc_convert_x(const TcParams &p, const GroupTable
         }
 }
 
+template <bool kCappedTables>
 __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_constant__ TcParams p) {
     using namespace sm100;
     extern __shared__ __align__(1024) uint8_t smem_raw_[];
@@ -258,7 +266,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
     const int nA = tc_aslots(T), ntmax = tc_ntmax(T), nR = p.nR;
     const int dcol0 = nA * 128, dset = 4 * ntmax;  // TMEM D set base and size
 
-    uint8_t *raw = smem + tc_raw_offset(T, K, p.E, no_dedup);
+    const int C = T * (K + 1), gcap = kCappedTables ? group_capacity(T, K, p.E, no_dedup) : C;
+    uint8_t *raw = smem + tc_raw_offset(T, K, gcap);
     uint8_t *bbuf = smem + TcSmem::bbuf;
     TcJob *jobs = reinterpret_cast<TcJob *>(smem + TcSmem::jobs);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + TcSmem::bars);
@@ -274,7 +283,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
     int *dn_per_ht_s = reinterpret_cast<int *>(smem + TcSmem::misc + 8);
     uint32_t *tile_ready_s = reinterpret_cast<uint32_t *>(smem + TcSmem::tile_ready);
     int32_t *tbl = reinterpret_cast<int32_t *>(smem + TcSmem::tables);
-    const int C = T * (K + 1), gcap = group_capacity(T, K, p.E, no_dedup);
     GroupTable tab{tbl, C, gcap};
     int *gu_prefix = tbl + tab.ints();
     int *dn_prefix = gu_prefix + (gcap + 1);
