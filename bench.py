@@ -47,12 +47,37 @@ KERNEL_SOURCES = ["moe_layer_decode_persistent_b300/csrc/api.cu",
                   "moe_layer_decode_persistent_b300/csrc/moe_common.cuh"]
 
 
+def _code_only(text: str) -> str:
+    """C/C++ source without comments and with whitespace collapsed, so that a
+    change of comments alone does not count as a change of the kernel."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        elif c in "\"'":  # string or character literal, copied as is
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash() -> str:
+    """Hash of the kernel sources' code (comments and whitespace ignored)."""
     h = hashlib.sha256()
     for p in KERNEL_SOURCES:
         fp = os.path.join(ROOT, p)
         if os.path.exists(fp):
-            h.update(open(fp, "rb").read())
+            h.update(_code_only(open(fp, encoding="utf-8").read()).encode())
     return h.hexdigest()[:16]
 
 

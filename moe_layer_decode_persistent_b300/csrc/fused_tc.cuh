@@ -17,9 +17,12 @@
 //     tile0 = rows ht*256.., tile1 = rows ht*256+128.., K = I chunk
 // Both tiles of a job share the B operand (the group's activation columns).
 //
-// Per CTA the roles are warp-specialised (26 warps):
+// Per CTA the roles are warp-specialised (18 warps; 26 with the two-parity
+// dequant build option):
 //   warp 0      producer: claims jobs, TMA-loads 128-byte-wide weight boxes
-//               (SWIZZLE_128B) and NVFP4 block scales into a 3-stage ring
+//               (SWIZZLE_128B) and NVFP4 block scales into a ring of 2 to 6
+//               stages (as many as shared memory holds next to the tables);
+//               at the end it watches the output tiles for the combine
 //   warp 1      B stager: copies the job's B tile per 128-K unit with
 //               cp.async (not the TMA queue, which is full of weight boxes), the
 //               f16 activation columns (gate/up; converted once per launch in
@@ -30,15 +33,15 @@
 //               one MMA per ~120 cycles whatever N is, so four issuers split
 //               each unit: issuer q takes tile q&1, K-steps of half q>>1, into
 //               its own accumulator (the halves are added in a fixed order)
-//   warps 6-21  dequant, four warpgroups (tile x unit parity), ping-ponged so
-//               one pair converts while the other synchronises: one thread
-//               per weight row, E2M1*E4M3 -> exact f16 (or E4M3 -> f16),
-//               written to TMEM as the MMA's A operand (the weights never
-//               touch shared memory as f16)
-//   warps 22-25 epilogue: TMEM accumulators -> registers; FP8 128x128 block
+//   warps 6-13  dequant, one warpgroup per tile: one thread per weight row,
+//               E2M1*E4M3 -> exact f16 (or E4M3 -> f16), written to TMEM as the
+//               MMA's A operand (the weights never touch shared memory as f16)
+//   warps 14-17 epilogue: TMEM accumulators -> registers; FP8 128x128 block
 //               scales applied per 128-K block in fp32; partial sums, the
-//               fixed-order reductions, SwiGLU, the f16 intermediate, and the
-//               final combine + single bf16 write
+//               fixed-order reductions, SwiGLU, the f16 intermediate, the down
+//               partials
+//   all warps   the final combine (fixed-order sum, single bf16 write), each
+//               warp as soon as its role is done
 //
 // Precision: weights dequantise exactly to f16 (e2m1*e4m3 has <= 6
 // significant bits); activations bf16 -> f16 (exact for |x| in [2^-17, 65504];
@@ -58,7 +61,9 @@ namespace moe {
 #ifndef MOE_TC_DQ_PARITIES
 #define MOE_TC_DQ_PARITIES 1
 #endif
-constexpr int kDqPar = MOE_TC_DQ_PARITIES;  // dequant warpgroups per tile (ping-pong when 2)
+// Dequant warpgroups per tile: 1, or 2 taking alternate units (a build option
+// that measured slower: 26 warps leave 72 registers and crowd the issuers).
+constexpr int kDqPar = MOE_TC_DQ_PARITIES;
 constexpr int kDqWarps = 8 * kDqPar;
 constexpr int kTcThreads = 32 * (2 + 4 + kDqWarps + 4);
 constexpr int kTcMaxT = 256;
@@ -656,7 +661,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
             }
         }
     } else if (warp < 2 + kIssuers + kDqWarps) {
-        // ===================== dequant (warps 6-21) =====================
+        // ===================== dequant (warps 6 .. 6+kDqWarps-1) =====================
         // warpgroup dq = (warp - 6) / 4: tile = dq & 1, parity = dq >> 1. A
         // warpgroup converts its tile's rows of the units whose running index
         // has its parity; it still steps through every unit and stage so its
@@ -778,7 +783,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
             if (!ok) break;
         }
     } else {
-        // ===================== epilogue (warps 14-17) =====================
+        // ===================== epilogue (the last 4 warps) =====================
         // Each warp owns 32 rows of the tile (its TMEM lane quarter) and runs
         // the reductions for those rows on its own: counters are kept per
         // (tile, quarter), so no warp ever waits for another.
