@@ -809,28 +809,39 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
             uint8_t *mb = p.midB + d.mid_off + (long long)d.tile * d.npad * 256;
             uint32_t range_bad = 0;
 
-            // phase 1, per 16-column chunk: the chunk's (gate, up) or (row h0, row h1)
-            // values -> partial sums, the intermediate, or the per-chunk down output
-            auto emit = [&](int cb, const float (&v0)[16], const float (&v1)[16]) {
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int c = cb + j;
-                    if (c >= d.n) continue;
+            // phase 1, one column at a time (a loop the compiler keeps rolled, so the
+            // epilogue's code stays small next to the dequant and MMA loops): the
+            // column's (gate, up) or (row h0, row h1) values from the D set -> partial
+            // sums, the intermediate, or the down output. With two K-halves per tile
+            // (NVFP4) they are added in a fixed order; FP8 jobs leave their promoted
+            // sum in K-half 0.
+            auto drain = [&](uint32_t dcol, bool halves) {
+#pragma unroll 1
+                for (int c = 0; c < d.n; ++c) {
+                    const uint32_t a0 = tmem_ld1(dcol + c), b0 = tmem_ld1(dcol + 2 * ntmax + c);
+                    uint32_t a1 = 0u, b1 = 0u;
+                    if (halves) {
+                        a1 = tmem_ld1(dcol + ntmax + c);
+                        b1 = tmem_ld1(dcol + 3 * ntmax + c);
+                    }
+                    tmem_wait_ld();
+                    const float v0 = halves ? __fadd_rn(__uint_as_float(a0), __uint_as_float(a1)) : __uint_as_float(a0);
+                    const float v1 = halves ? __fadd_rn(__uint_as_float(b0), __uint_as_float(b1)) : __uint_as_float(b0);
                     const size_t col = (size_t)(d.col0 + c);
                     if (d.kind == 0) {
                         if (d.nkc > 1) {
-                            p.P[(((size_t)d.kc * 2 + 0) * p.Ucap + col) * p.Imax + i] = v0[j];
-                            p.P[(((size_t)d.kc * 2 + 1) * p.Ucap + col) * p.Imax + i] = v1[j];
+                            p.P[(((size_t)d.kc * 2 + 0) * p.Ucap + col) * p.Imax + i] = v0;
+                            p.P[(((size_t)d.kc * 2 + 1) * p.Ucap + col) * p.Imax + i] = v1;
                         } else {
-                            const float m = __fmul_rn(silu_f32(__fmul_rn(v0[j], gs13)), __fmul_rn(v1[j], gs13));
+                            const float m = __fmul_rn(silu_f32(__fmul_rn(v0, gs13)), __fmul_rn(v1, gs13));
                             const __half hm = __float2half_rn(m);
                             if (__hisinf(hm) || !(fabsf(m) == fabsf(m))) range_bad = 1;
                             *reinterpret_cast<__half *>(mb + b_off(c, r)) = hm;
                         }
                     } else {
                         float *y = p.Y + ((size_t)d.kc * p.Ucap + col) * H;
-                        if (h0 < H) y[h0] = v0[j];
-                        if (h1 < H) y[h1] = v1[j];
+                        if (h0 < H) y[h0] = v0;
+                        if (h1 < H) y[h1] = v1;
                     }
                 }
             };
@@ -871,6 +882,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                         for (int j = 0; j < 8; ++j)
                             acc1[h8 + j] = __fmaf_rn(s1, __fadd_rn(__uint_as_float(x0[j]), __uint_as_float(x1[j])), acc1[h8 + j]);
                     }
+                    if (u == d.nunits - 1) {
+                        // the promoted sums go back to K-half 0 of this D set and are
+                        // drained from there before the set is released
+                        uint32_t o0[16], o1[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            o0[j] = __float_as_uint(acc0[j]);
+                            o1[j] = __float_as_uint(acc1[j]);
+                        }
+                        tmem_st16(dcol, o0);
+                        tmem_st16(dcol + 2 * ntmax, o1);
+                        tmem_wait_st();
+                        drain(dcol, false);
+                    }
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&dempty[ds]);
@@ -880,32 +905,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                     }
                 }
                 if (!ok) break;
-                emit(0, acc0, acc1);
             } else {
                 if (!__all_sync(0xffffffffu, mbar_wait(&dfull[ds], dph, abort_flag, err))) break;
                 tc_fence_after();
-                const uint32_t dcol = tmem + lane_base + dcol0 + ds * dset;
-#pragma unroll 1
-                for (int cb = 0; cb < d.npad; cb += 16) {
-                    float v0[16], v1[16];
-                    {
-                        uint32_t x0[16], x1[16];
-                        tmem_ld16(dcol + cb, x0);
-                        tmem_ld16(dcol + ntmax + cb, x1);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) v0[j] = __fadd_rn(__uint_as_float(x0[j]), __uint_as_float(x1[j]));
-                    }
-                    {
-                        uint32_t x0[16], x1[16];
-                        tmem_ld16(dcol + 2 * ntmax + cb, x0);
-                        tmem_ld16(dcol + 3 * ntmax + cb, x1);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) v1[j] = __fadd_rn(__uint_as_float(x0[j]), __uint_as_float(x1[j]));
-                    }
-                    emit(cb, v0, v1);
-                }
+                drain(tmem + lane_base + dcol0 + ds * dset, true);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&dempty[ds]);

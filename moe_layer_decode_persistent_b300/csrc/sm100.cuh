@@ -64,9 +64,10 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
 // parked in the hardware (it does not spin on the issue slots the working
 // warps need). Gives up after the wait budget (or at once when *abort is
 // already set), sets the timeout bit in *err and *abort, and returns false.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
-                                          uint32_t *err) {
-    if (mbar_try_wait(bar, parity)) return true;
+// The waiting part lives out of line: it is the same at every call site and
+// rarely on the fast path, and keeping it out of the loops that call it keeps
+// the kernel's hot code small enough for the instruction cache.
+__device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, volatile int *abort, uint32_t *err) {
     const unsigned long long t0 = globaltimer_ns();
     while (true) {
         if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
@@ -77,6 +78,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
             return false;
         }
     }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                          uint32_t *err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, 1000u)) return true;  // most waits end here
+    return mbar_wait_slow(bar, parity, abort, err);
 }
 
 // ---- proxies and async copies -------------------------------------------
@@ -189,6 +197,13 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 }
 
 // Warp-wide: each thread loads 8 consecutive 32-bit columns of its lane.
+// One 32-bit column of this warp's 32 TMEM lanes: lane l gets lane l's value.
+__device__ __forceinline__ uint32_t tmem_ld1(uint32_t taddr) {
+    uint32_t v;
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(v) : "r"(taddr) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
