@@ -33,18 +33,23 @@ moe_status cuda_fail(cudaError_t e, const char *what) {
 }
 
 constexpr int kMaxT = 256, kMaxK = 16, kMaxE = 1024, kMaxDim = 16384;
+static_assert(kMaxT * (kMaxK + 1) <= moe::kTcReadyCap, "group_ready capacity");
+static_assert(kMaxDim / 256 <= moe::kTcHtileCap, "htile_cnt capacity");
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-// Workspace. Both kernels share the 256-byte header (error word, counters).
-//   CUDA-core path : header | mid fp32 [Ucap][Imax] | y fp32 [Ucap][H]
-//   tensor path    : header | group_ready [C] | x_ready [C] |
-//                    tile_cnt [C*Imax/128*4] | htile_cnt [H/256*4] | P | Y | midB | xB
+// Workspace. Both kernels share the 256-byte header (error word, counters),
+// and the tensor path's counters come next in a region the CUDA-core path never
+// writes, so they stay valid when the two paths take turns on one workspace:
+//   header | group_ready [2][kTcReadyCap] | htile_cnt [2][kTcHtileCap] |
+//   tile_cnt [C*Imax/128*4] | then
+//   CUDA-core path : mid fp32 [Ucap][Imax] | y fp32 [Ucap][H]
+//   tensor path    : P | Y | midB | xh f16 [T][H]
 // followed by the host-buffer call's staging area. Ucap = C = T*(K+1).
 struct WsLayout {
     size_t mid = 0, y = 0, fma_end = 0;
-    size_t tc_ready = 0, tc_xready = 0, tc_tile = 0, tc_htile = 0, tc_ctrl_end = 0, tc_P = 0, tc_Y = 0,
-           tc_midB = 0, tc_xB = 0, tc_end = 0;
+    size_t tc_ready = 0, tc_htile = 0, tc_tile = 0, tc_ctrl_end = 0, tc_P = 0, tc_Y = 0, tc_midB = 0,
+           tc_xh = 0, tc_end = 0;
     size_t dev_total = 0;
     size_t st_x = 0, st_ids = 0, st_w = 0, st_out = 0, host_total = 0;
 };
@@ -56,22 +61,21 @@ WsLayout ws_layout(const moe_shape *s) {
     const size_t Imax = (size_t)std::max(s->I, s->I_shared);
     const size_t H = (size_t)s->H;
     size_t off = sizeof(moe::WsHeader);
-    L.mid = off = align_up(off, 256);
+    L.tc_ready = off;
+    off += 2 * (size_t)moe::kTcReadyCap * 4;
+    L.tc_htile = off = align_up(off, 16);
+    off += 2 * (size_t)moe::kTcHtileCap * 4;
+    L.tc_tile = off = align_up(off, 16);
+    off += Ucap * (Imax / 128) * 4 * 4;
+    L.tc_ctrl_end = off = align_up(off, 256);
+
+    L.mid = off;
     off += Ucap * Imax * sizeof(float);
     L.y = off = align_up(off, 256);
     off += Ucap * H * sizeof(float);
     L.fma_end = align_up(off, 256);
 
-    off = sizeof(moe::WsHeader);
-    L.tc_ready = off;
-    off += Ucap * 4;
-    L.tc_xready = off = align_up(off, 16);
-    off += Ucap * 4;
-    L.tc_tile = off = align_up(off, 16);
-    off += Ucap * (Imax / 128) * 4 * 4;
-    L.tc_htile = off = align_up(off, 16);
-    off += ((H + 255) / 256) * 4 * 4;
-    L.tc_ctrl_end = off = align_up(off, 256);
+    off = L.tc_ctrl_end;
     const int Ti = (int)T, Hi = (int)H;
     const size_t nkc_gu = Ti <= moe::kSplitMaxT
                               ? (size_t)std::max(moe::tc_nkc_gu(moe::kFmtNvfp4, Hi, Ti),
@@ -87,8 +91,8 @@ WsLayout ws_layout(const moe_shape *s) {
     const size_t cols_padded = 16 * Ucap;
     L.tc_midB = off = align_up(off, 256);
     off += cols_padded * (Imax / 128) * 256;
-    L.tc_xB = off = align_up(off, 256);
-    off += cols_padded * H * 2;
+    L.tc_xh = off = align_up(off, 256);
+    off += T * H * 2;
     L.tc_end = align_up(off, 256);
 
     L.dev_total = off = std::max(L.fma_end, L.tc_end);
@@ -415,8 +419,7 @@ moe_status launch_fused_tc(const moe::FusedParams &fp, const WsLayout &L, const 
     p.P = reinterpret_cast<float *>(ws + L.tc_P);
     p.Y = reinterpret_cast<float *>(ws + L.tc_Y);
     p.midB = reinterpret_cast<uint8_t *>(ws + L.tc_midB);
-    p.xB = reinterpret_cast<uint8_t *>(ws + L.tc_xB);
-    p.x_ready = reinterpret_cast<uint32_t *>(ws + L.tc_xready);
+    p.xh = reinterpret_cast<__half *>(ws + L.tc_xh);
     p.Ucap = s->T * (s->K + 1);
     p.Imax = std::max(s->I, s->I_shared);
     // the raw weight ring gets as many stages as shared memory holds

@@ -24,10 +24,11 @@
 //               stages (as many as shared memory holds next to the tables);
 //               at the end it watches the output tiles for the combine
 //   warp 1      B stager: copies the job's B tile per 128-K unit with
-//               cp.async (not the TMA queue, which is full of weight boxes), the
-//               f16 activation columns (gate/up; converted once per launch in
-//               the prologue, spread over all CTAs) or the f16 intermediate
-//               (down), after waiting for its producers
+//               cp.async (not the TMA queue, which is full of weight boxes):
+//               gate/up gathers each column from its row of the f16
+//               activations (converted once per launch at the start, spread
+//               over all CTAs); down copies the f16 intermediate. It first
+//               waits for the operand's producers.
 //   warps 2-5   MMA issuers: tcgen05.mma kind::f16, M=128, N=16|32, K=16,
 //               A from TMEM, B from shared memory. One issuing thread sustains
 //               one MMA per ~120 cycles whatever N is, so four issuers split
@@ -93,6 +94,9 @@ constexpr int kKcFp8 = 1024;
 constexpr int kKcDown = 1024;
 constexpr int kSplitMaxT = 16;
 constexpr int kCombBatch = 20;  // combine: partial sums loaded per batch (18 for DSv3 shapes at T <= 16)
+// Launch-wide counters, two sets used in alternate launches (by parity).
+constexpr int kTcReadyCap = 256 * 17;  // (group, column tile) pairs: at most T*(K+1)
+constexpr int kTcHtileCap = 64;        // 256-row output tiles: H / 256 at most
 
 struct TcMaps {
     CUtensorMap r13, r13s, r2, r2s, s13, s13s, s2, s2s;
@@ -109,14 +113,13 @@ struct TcParams {
     int nR;  // raw weight ring stages (kRawStagesMin..kRawStagesMax)
     unsigned flags;
     WsHeader *hdr;
-    uint32_t *group_ready;  // per (group, column tile)
-    uint32_t *tile_cnt;     // per (group, column tile, 128-row tile)
-    uint32_t *htile_cnt;    // per 256-row output tile
+    uint32_t *group_ready;  // [2][kTcReadyCap], per parity, per (group, column tile)
+    uint32_t *tile_cnt;     // per (group, column tile, 128-row tile); each launch leaves it zero
+    uint32_t *htile_cnt;    // [2][kTcHtileCap], per parity, per 256-row output tile
     float *P;               // gate/up partials [kc][2][Ucap][Imax]
     float *Y;               // down partials [kc][Ucap][H]
     uint8_t *midB;          // f16 intermediate in MMA B layout
-    uint8_t *xB;            // activation columns, f16, MMA B layout per (group, column tile)
-    uint32_t *x_ready;      // per (group, column tile): columns converted
+    __half *xh;             // the activations as f16 [T][H]
     int Ucap, Imax;
 };
 
@@ -129,7 +132,6 @@ struct TcJob {
     int rows0, rows1;
     int tile_id, pair;
     long long mid_off;  // bytes into midB of this (group, column tile)
-    long long x_off;    // bytes into xB of this (group, column tile)
 };
 
 // ---- per-launch constants shared by host and device -----------------------
@@ -161,11 +163,11 @@ struct TcSmem {
     static constexpr int bars = jobs + kJobSlots * (int)sizeof(TcJob);
     // jfull, jempty, rfull, rempty, sfull, sempty, dfull, dempty, drain[4]
     static constexpr int nbars = 2 * kJobSlots + 2 * kRawStagesMax + 2 * kASlotsMax + 2 * 2 + kIssuers;
-    static constexpr int misc = bars + nbars * 8;  // tmem addr, abort, flags
+    static constexpr int misc = bars + nbars * 8;  // tmem addr, abort, down jobs per tile, parity
     static constexpr int tile_ready = misc + 64;   // per 256-row output tile: combine may start (64 max)
     static constexpr int tables = tile_ready + 256;  // group table, then per-group arrays
 };
-constexpr int kTcGroupArrays = 6;  // gu, dn, tile, mid, pair and x-column prefix sums
+constexpr int kTcGroupArrays = 5;  // gu, dn, tile, mid and pair prefix sums
 
 // The group table (per-group arrays of capacity gcap), the per-group prefix
 // sums (gcap + 1 each), then two float arrays of C = T*(K+1): each (row, slot)'s
@@ -201,41 +203,26 @@ __device__ __forceinline__ int group_of_col(const int32_t *g0, int G, int c) {
     return lo;
 }
 
-// This CTA's share of the activation columns (column c goes to CTA c mod grid)
-// -> f16 in the MMA B layout of its (group, column tile); each converted column
-// is then counted in x_ready. Whole CTA calls.
-__device__ __forceinline__ void tc_convert_x(const TcParams &p, const GroupTable &tab, const int *xcol_prefix,
-                                             const int *pair_prefix) {
-    const int ctid = threadIdx.x, nthr = blockDim.x;
-    const int T = p.T, H = p.H, G = tab.G(), U = tab.U();
-    const int32_t *gexp = tab.gexp(), *gn = tab.gncols(), *g0 = tab.gcol0();
-    const int32_t *crow = tab.col_row();
-    const int per_col = H / 8;  // 16-byte items of one column
-    const int b = (int)blockIdx.x, nb = (int)gridDim.x;
-    const int ncols = U > b ? (U - 1 - b) / nb + 1 : 0;
-    const int nitems = ncols * per_col;
+// The activations -> f16 [T][H], the gate/up MMA's B operand (bf16 -> f16 is
+// exact for |x| in [2^-17, 65504]; larger magnitudes set MOE_DEV_RANGE). The
+// 16-byte items are dealt over `nthr` threads of the grid (this one is `gt`),
+// four loads in flight per thread.
+__device__ __forceinline__ void tc_convert_x(const TcParams &p, int gt, int nthr) {
+    const int n = p.T * p.H / 8;
+    const uint4 *src = reinterpret_cast<const uint4 *>(p.x);
+    uint4 *dst = reinterpret_cast<uint4 *>(p.xh);
     uint32_t range_bad = 0;
-    for (int i0 = ctid; i0 < nitems; i0 += 4 * nthr) {
+    for (int i0 = gt; i0 < n; i0 += 4 * nthr) {
         uint4 v[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {  // the loads first, so they are in flight together
+        for (int j = 0; j < 4; ++j) {
             const int it = i0 + j * nthr;
-            v[j] = make_uint4(0u, 0u, 0u, 0u);
-            if (it < nitems) {
-                const int c = b + (it / per_col) * nb;
-                v[j] = __ldg(reinterpret_cast<const uint4 *>(p.x + (size_t)crow[c] * H) + it % per_col);
-            }
+            v[j] = it < n ? __ldg(src + it) : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int it = i0 + j * nthr;
-            if (it >= nitems) break;
-            const int c = b + (it / per_col) * nb, k8i = it % per_col;
-            const int g = group_of_col(g0, G, c);
-            const int nt = tc_nt(gexp[g] < 0 ? p.shared.fmt : p.routed.fmt, T);
-            const int ct = (c - g0[g]) / nt, cl = (c - g0[g]) % nt;
-            const int n = min(nt, gn[g] - ct * nt), npad = ((n + 15) / 16) * 16;
-            uint8_t *base = p.xB + ((long long)xcol_prefix[g] + (long long)ct * nt) * H * 2;
+            if (it >= n) break;
             const uint32_t w4[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
             uint32_t o[4];
 #pragma unroll
@@ -244,20 +231,10 @@ __device__ __forceinline__ void tc_convert_x(const TcParams &p, const GroupTable
                 if (__hisinf(__low2half(h)) || __hisinf(__high2half(h))) range_bad = 1;
                 o[k] = pack_h2(h);
             }
-            *reinterpret_cast<uint4 *>(base + (long long)(k8i >> 4) * npad * 256 + b_off(cl, (k8i & 15) * 8)) =
-                make_uint4(o[0], o[1], o[2], o[3]);
+            dst[it] = make_uint4(o[0], o[1], o[2], o[3]);
         }
     }
     if (range_bad) atomicOr(&p.hdr->err, kErrRange);
-    __threadfence();
-    __syncthreads();
-    if (ctid == 0)
-        for (int k = 0; k < ncols; ++k) {
-            const int c = b + k * nb;
-            const int g = group_of_col(g0, G, c);
-            const int nt = tc_nt(gexp[g] < 0 ? p.shared.fmt : p.routed.fmt, T);
-            red_add_release_gpu(p.x_ready + pair_prefix[g] + (c - g0[g]) / nt, 1u);
-        }
 }
 
 template <bool kCappedTables>
@@ -286,6 +263,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
     uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(smem + TcSmem::misc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + TcSmem::misc + 4);
     int *dn_per_ht_s = reinterpret_cast<int *>(smem + TcSmem::misc + 8);
+    int *par_s = reinterpret_cast<int *>(smem + TcSmem::misc + 12);
     uint32_t *tile_ready_s = reinterpret_cast<uint32_t *>(smem + TcSmem::tile_ready);
     int32_t *tbl = reinterpret_cast<int32_t *>(smem + TcSmem::tables);
     GroupTable tab{tbl, C, gcap};
@@ -294,22 +272,68 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
     int *tile_prefix = dn_prefix + (gcap + 1);
     int *mid_prefix = tile_prefix + (gcap + 1);
     int *pair_prefix = mid_prefix + (gcap + 1);
-    int *xcol_prefix = pair_prefix + (gcap + 1);
-    float *comb_w = reinterpret_cast<float *>(xcol_prefix + (gcap + 1));  // [T][K+1]
+    float *comb_w = reinterpret_cast<float *>(pair_prefix + (gcap + 1));  // [T][K+1]
     float *comb_g = comb_w + C;                                        // [T][K+1]
     uint32_t *err = &p.hdr->err;
 
-    // ---- prologue: group table (scratch aliases the raw ring), per-group sums
+    // ---- prologue -----------------------------------------------------------
+    // Warp 0 (the producer) sets up the barriers, helps build the group table,
+    // sums the per-group job counts and starts streaming weights at once; the
+    // other warps convert the activations meanwhile, then fill the combine
+    // coefficients, then take up their roles.
+    const int nw1 = kTcThreads - 32;  // threads of warps 1..
+    if (warp == 0 && lane == 0) {
+        for (int i = 0; i < kJobSlots; ++i) {
+            mbar_init(&jfull[i], 1);
+            mbar_init(&jempty[i], 1 + kIssuers + kDqWarps + 4);  // stager, issuers, dequant, epilogue
+        }
+        for (int i = 0; i < kRawStagesMax; ++i) {
+            mbar_init(&rfull[i], 1);
+            mbar_init(&rempty[i], kDqWarps);
+        }
+        for (int i = 0; i < kASlotsMax; ++i) {
+            mbar_init(&sfull[i], 8 + 32);  // 8 dequant warps + one cp.async arrival per stager lane
+            mbar_init(&sempty[i], kIssuers);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&dfull[i], kIssuers);
+            mbar_init(&dempty[i], 4);
+        }
+        for (int i = 0; i < kIssuers; ++i) mbar_init(&drain[i], 1);
+        for (int i = 0; i < 64; ++i) tile_ready_s[i] = 0;
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    uint32_t start_no = 0;
+    if (warp == 1) {
+        tmem_alloc(tmem_base_s, kTmemCols);
+        tc_fence_before();
+        // this launch's parity: CTA starts are counted modulo 2 * grid (the
+        // result is used after the conversion's loads are in flight)
+        if (lane == 0) start_no = atomicInc(&p.hdr->start_cnt, 2u * gridDim.x - 1u);
+    }
+    if (warp >= 1) tc_convert_x(p, (tid - 32) * (int)gridDim.x + (int)blockIdx.x, nw1 * (int)gridDim.x);
+    if (tid == 32) *par_s = (int)(start_no / gridDim.x);
+
+    // group table (its scratch aliases the raw ring; it ends with a CTA barrier,
+    // which also publishes the barriers, the parity and the TMEM address)
     group_table_cta(p.ids, T, K, p.E, no_dedup, tab, reinterpret_cast<int *>(raw),
                     blockIdx.x == 0 ? err : nullptr);
     const int G = tab.G();
     const int32_t *gexp = tab.gexp(), *gn = tab.gncols(), *g0 = tab.gcol0(), *rcol = tab.row_col();
     const int *crow = tab.col_row();
+    const int par = *par_s;
+    uint32_t *group_ready = p.group_ready + par * kTcReadyCap;
+    uint32_t *htile_cnt = p.htile_cnt + par * kTcHtileCap;
+    if (tid == 32) {  // this CTA's activation slice is converted (the table's barriers ordered it)
+        __threadfence();
+        red_add_release_gpu(&p.hdr->x_ready[par], 1u);
+    }
     if (warp == 0) {
-        int run[6] = {0, 0, 0, 0, 0, 0};
+        int run[5] = {0, 0, 0, 0, 0};
         for (int base = 0; base < G; base += 32) {
             const int g = base + lane;
-            int v[6] = {0, 0, 0, 0, 0, 0};  // gu jobs, dn jobs, tiles, mid units, pairs, x columns
+            int v[5] = {0, 0, 0, 0, 0};  // gu jobs, dn jobs, tiles, mid units, pairs
             if (g < G) {
                 const bool sh = gexp[g] < 0;
                 const int fmt = sh ? p.shared.fmt : p.routed.fmt;
@@ -324,15 +348,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                 v[2] = nct * tiles;
                 v[3] = np * tiles;
                 v[4] = nct;
-                v[5] = np;
             }
-            int sc[6];
+            int sc[5];
 #pragma unroll
-            for (int a = 0; a < 6; ++a) sc[a] = v[a];
+            for (int a = 0; a < 5; ++a) sc[a] = v[a];
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
 #pragma unroll
-                for (int a = 0; a < 6; ++a) {
+                for (int a = 0; a < 5; ++a) {
                     const int y = __shfl_up_sync(0xffffffffu, sc[a], o);
                     if (lane >= o) sc[a] += y;
                 }
@@ -343,10 +366,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                 tile_prefix[g] = run[2] + sc[2] - v[2];
                 mid_prefix[g] = run[3] + sc[3] - v[3];
                 pair_prefix[g] = run[4] + sc[4] - v[4];
-                xcol_prefix[g] = run[5] + sc[5] - v[5];
             }
 #pragma unroll
-            for (int a = 0; a < 6; ++a) run[a] += __shfl_sync(0xffffffffu, sc[a], 31);
+            for (int a = 0; a < 5; ++a) run[a] += __shfl_sync(0xffffffffu, sc[a], 31);
         }
         if (lane == 0) {
             gu_prefix[G] = run[0];
@@ -354,42 +376,34 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
             tile_prefix[G] = run[2];
             mid_prefix[G] = run[3];
             pair_prefix[G] = run[4];
-            xcol_prefix[G] = run[5];
-            for (int i = 0; i < kJobSlots; ++i) {
-                mbar_init(&jfull[i], 1);
-                mbar_init(&jempty[i], 1 + kIssuers + kDqWarps + 4);  // stager, issuers, dequant, epilogue
-            }
-            for (int i = 0; i < kRawStagesMax; ++i) {
-                mbar_init(&rfull[i], 1);
-                mbar_init(&rempty[i], kDqWarps);
-            }
-            for (int i = 0; i < kASlotsMax; ++i) {
-                mbar_init(&sfull[i], 8 + 32);  // 8 dequant warps + one cp.async arrival per stager lane
-                mbar_init(&sempty[i], kIssuers);
-            }
-            for (int i = 0; i < 2; ++i) {
-                mbar_init(&dfull[i], kIssuers);
-                mbar_init(&dempty[i], 4);
-            }
-            for (int i = 0; i < kIssuers; ++i) mbar_init(&drain[i], 1);
-            for (int i = 0; i < 64; ++i) tile_ready_s[i] = 0;
-            *abort_flag = 0;
             int dph_total = 0;  // down jobs that write one 256-row output tile
             for (int g = 0; g < G; ++g) {
                 const bool sh = gexp[g] < 0;
                 const int nt = tc_nt(sh ? p.shared.fmt : p.routed.fmt, T);
                 dph_total += ((gn[g] + nt - 1) / nt) * tc_nkc_dn(sh ? p.Is : p.I, T);
             }
+            // read by the other warps after their first job-slot wait
             *dn_per_ht_s = dph_total;
-            fence_mbar_init();
         }
-    }
-    if (warp == 1) tmem_alloc(tmem_base_s, kTmemCols);
-    if (warp >= 2) {
+        __syncwarp();
+    } else {
+        // zero the other parity's counters for the next launch (the launch
+        // before this one was their last user)
+        {
+            const int opar = par ^ 1;
+            const int gt = (int)blockIdx.x * nw1 + (tid - 32);
+            const int nz = kTcReadyCap + kTcHtileCap + 2;
+            for (int i = gt; i < nz; i += nw1 * (int)gridDim.x) {
+                if (i < kTcReadyCap) p.group_ready[opar * kTcReadyCap + i] = 0u;
+                else if (i < kTcReadyCap + kTcHtileCap) p.htile_cnt[opar * kTcHtileCap + i - kTcReadyCap] = 0u;
+                else if (i == kTcReadyCap + kTcHtileCap) p.hdr->job_next[opar] = 0u;
+                else p.hdr->x_ready[opar] = 0u;
+            }
+        }
         // combine coefficients of every (row, slot): weight 1 and the shared
         // down scale for slot 0, the router weight and the expert's down scale
         // for pick slots
-        for (int i = tid - 64; i < C; i += kTcThreads - 64) {
+        for (int i = tid - 32; i < C; i += nw1) {
             const int t = i / (K + 1), q = i - t * (K + 1);
             float w = 1.0f, gsc = 1.0f;
             if (q == 0) {
@@ -403,27 +417,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
             comb_w[i] = w;
             comb_g[i] = gsc;
         }
+        named_bar_sync(1, nw1);  // the coefficients, among warps 1..
+        tc_fence_after();
     }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
     const uint32_t tmem = *tmem_base_s;
-    const int NGU = gu_prefix[G], NDN = dn_prefix[G];
-    const int njobs = NGU + NDN;
-    const int dn_per_ht = *dn_per_ht_s;
 
-    tc_convert_x(p, tab, xcol_prefix, pair_prefix);
     auto job_at = [&](int slot) -> TcJob { return jobs[slot]; };
 
     if (warp == 0) {
         // ===================== producer =====================
         if (lane == 0) {
+            const int NGU = gu_prefix[G], njobs = NGU + dn_prefix[G];
             int js = 0, jph = 0, rs = 0, rph = 0;
             int cur_gu = 0, cur_dn = 0;
             uint32_t armed = 0;  // raw stages with a TMA in flight not yet seen consumed
-            for (;;) {
+            // CTA b takes job b first, with no claim; later jobs come from the counter
+            int j = (int)blockIdx.x;
+            for (;; j = (int)gridDim.x + (int)atomicAdd(&p.hdr->job_next[par], 1u)) {
                 TcJob d;
-                const int j = (int)atomicAdd(&p.hdr->job_next, 1u);
                 if (*abort_flag || j >= njobs) {
                     d.kind = -1;
                 } else {
@@ -480,7 +491,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                     d.tile_id = tile_prefix[g] + d.ct * tiles + (d.kind == 0 ? d.tile : 0);
                     d.pair = pair_prefix[g] + d.ct;
                     d.mid_off = ((long long)mid_prefix[g] + (long long)d.ct * tiles * nt) * 256ll;
-                    d.x_off = ((long long)xcol_prefix[g] + (long long)d.ct * nt) * H * 2;
                 }
                 if (!mbar_wait(&jempty[js], jph ^ 1, abort_flag, err)) break;
                 jobs[js] = d;
@@ -544,6 +554,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
         // ===================== B stager =====================
         int js = 0, jph = 0, bs = 0, bph = 0;  // unit slot ring position
         const uint32_t bunit = (uint32_t)ntmax * kUnitK * 2;  // bytes of one B buffer
+        const int nl = lane & 7, kq = lane >> 3;  // gather: column within an 8-column block, K quarter
+        bool x_seen = false;
         for (;;) {
             if (!__all_sync(0xffffffffu, mbar_wait(&jfull[js], jph, abort_flag, err))) break;
             const TcJob d = job_at(js);
@@ -554,13 +566,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                 jph ^= 1;
             }
             if (d.kind < 0) break;
-            // wait until the B operand's producers are done: the converted
-            // activation columns (gate/up) or every quarter of every row tile
-            // of the group's intermediate (down)
+            // wait until the B operand's producers are done: every CTA's slice
+            // of the activations (gate/up; once per launch) or every quarter of
+            // every row tile of the group's intermediate (down)
             int okl = 1;
-            if (lane == 0) {
-                const uint32_t need = d.kind == 0 ? (uint32_t)d.n : (uint32_t)(4 * (d.Ig / 128));
-                const uint32_t *flag = (d.kind == 0 ? p.x_ready : p.group_ready) + d.pair;
+            if (lane == 0 && !(d.kind == 0 && x_seen)) {
+                const uint32_t need = d.kind == 0 ? gridDim.x : (uint32_t)(4 * (d.Ig / 128));
+                const uint32_t *flag = d.kind == 0 ? &p.hdr->x_ready[par] : group_ready + d.pair;
                 if (ld_acquire_gpu(flag) < need) {
                     const unsigned long long t0 = globaltimer_ns();
                     while (ld_acquire_gpu(flag) < need) {
@@ -581,8 +593,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
             // the other lanes' copies below are ordered after lane 0's acquire
             bool ok = __shfl_sync(0xffffffffu, okl, 0) != 0;
             __syncwarp();
+            if (d.kind == 0) x_seen = true;
+            // gate/up: this lane's columns nb*8 + nl (nb < npad/8) come from
+            // their rows of xh and the padding columns are zero-filled without
+            // a read (many lanes reading one address slows the copies down);
+            // down: the contiguous intermediate
+            const __half *xrow[kNt / 8];
+#pragma unroll
+            for (int nb = 0; nb < kNt / 8; ++nb)
+                xrow[nb] = p.xh + (size_t)crow[d.col0 + min(nb * 8 + nl, d.n - 1)] * H + kq * 8;
             const uint32_t bytes = (uint32_t)d.npad * 256u;
-            const uint8_t *src0 = d.kind == 0 ? p.xB + d.x_off : p.midB + d.mid_off;
+            const uint8_t *mid0 = p.midB + d.mid_off;
             for (int u = 0; u < d.nunits && ok; ++u) {
                 if (!__all_sync(0xffffffffu, mbar_wait(&sempty[bs], bph ^ 1, abort_flag, err))) {
                     ok = false;
@@ -590,9 +611,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                 }
                 {
                     const int ku = d.k0 / kUnitK + u;  // global K unit index
-                    const uint8_t *src = src0 + (long long)ku * bytes;
                     uint8_t *dst = bbuf + bs * bunit;
-                    for (uint32_t o = (uint32_t)lane * 16; o < bytes; o += 32 * 16) cp_async16(dst + o, src + o);
+                    if (d.kind == 0) {
+                        // B layout: core matrices of 8 columns x 8 K, 2048 B per 8 columns
+                        uint8_t *dl = dst + kq * 128 + nl * 16;
+#pragma unroll
+                        for (int nb = 0; nb < kNt / 8; ++nb)
+                            if (nb < d.npad / 8)
+#pragma unroll
+                                for (int m = 0; m < 4; ++m)
+                                    cp_async16_zfill(dl + nb * 2048 + m * 512, xrow[nb] + ku * kUnitK + m * 32,
+                                                     nb * 8 + nl < d.n ? 16u : 0u);
+                    } else {
+                        const uint8_t *src = mid0 + (long long)ku * bytes;
+                        for (uint32_t o = (uint32_t)lane * 16; o < bytes; o += 32 * 16) cp_async16(dst + o, src + o);
+                    }
                     cp_async_arrive_noinc(&sfull[bs]);
                 }
                 if (++bs == nA) {
@@ -951,14 +984,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                 if (have_mid) {
                     __threadfence();
                     __syncwarp();
-                    if (lane == 0) atom_add_acq_rel_gpu(p.group_ready + d.pair, 1u);
+                    if (lane == 0) atom_add_acq_rel_gpu(group_ready + d.pair, 1u);
                 }
             } else {
                 // ---- down phase 2: count this (job, quarter) on its 256-row tile;
                 // the tile is combined once every down job has arrived ----
                 __threadfence();
                 __syncwarp();
-                if (lane == 0) atom_add_acq_rel_gpu(p.htile_cnt + d.tile, 1u);
+                if (lane == 0) atom_add_acq_rel_gpu(htile_cnt + d.tile, 1u);
             }
         }
     }
@@ -967,7 +1000,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
     __syncwarp();
 
     // ---- combine: every warp of the grid shares the output ------------------
-    // A 256-row output tile is complete once all 4*dn_per_ht (down job,
+    // A 256-row output tile is complete once all 4 * (down jobs per tile) (down job,
     // quarter) arrivals are in. Warp 0 (the producer, which finishes first)
     // watches every tile's counter with one load per lane per round and marks
     // the complete ones in shared memory; the other warps start on the combine
@@ -980,33 +1013,33 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
     // each y the sum of its K-chunk partials in chunk order. The partials are
     // loaded kCombBatch at a time with no dependence between them, so a unit
     // costs about one memory round trip.
-    const uint32_t tile_target = 4u * (uint32_t)dn_per_ht;
+    const uint32_t tile_target = 4u * (uint32_t)*dn_per_ht_s;
     if (warp == 0) {
         const int nht = H / 256;  // <= 64
         uint32_t pending = (lane < nht ? 1u : 0u) | (lane + 32 < nht ? 2u : 0u);
         const unsigned long long t0 = globaltimer_ns();
-        unsigned nap = 128;
-        while (!*abort_flag) {
+        // one memory round trip per round: the error word (another CTA gave up)
+        // and the clock are looked at every 8th round only
+        for (unsigned round = 1; !*abort_flag; ++round) {
 #pragma unroll
             for (int k = 0; k < 2; ++k)
                 if ((pending >> k) & 1u) {
                     const int ht = lane + 32 * k;
-                    if (ld_acquire_gpu(p.htile_cnt + ht) >= tile_target) {
+                    if (ld_acquire_gpu(htile_cnt + ht) >= tile_target) {
                         st_release_cta_shared(tile_ready_s + ht, 1u);
                         pending &= ~(1u << k);
                     }
                 }
             if (!__any_sync(0xffffffffu, pending != 0u)) break;
-            if ((*reinterpret_cast<volatile uint32_t *>(err) & kErrWaitTimeout) ||
-                globaltimer_ns() - t0 > kWaitBudgetNs) {
+            if ((round & 7u) == 0u && ((*reinterpret_cast<volatile uint32_t *>(err) & kErrWaitTimeout) ||
+                                       globaltimer_ns() - t0 > kWaitBudgetNs)) {
                 if (lane == 0) {
                     atomicOr(err, kErrWaitTimeout);
                     *abort_flag = 1;
                 }
                 break;
             }
-            __nanosleep(nap);
-            if (nap < 512) nap <<= 1;
+            __nanosleep(128);
         }
         __syncwarp();
     } else if (!*abort_flag) {
@@ -1017,6 +1050,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
         for (long long wu = (long long)(warp - 1) * gridDim.x + blockIdx.x; wu < nwu;
              wu += (long long)gridDim.x * ncw) {
             const int t = (int)(wu / hw), h = (int)(wu % hw) * 32 + lane, ht = h >> 8;
+            float acc = __bfloat162float(p.x[(size_t)t * H + h]);  // the residual, before the wait
             if (!ld_acquire_cta_shared(tile_ready_s + ht)) {
                 const unsigned long long t0 = globaltimer_ns();
                 bool ready = false;
@@ -1031,7 +1065,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
             }
             const int32_t *rc = rcol + t * (K + 1);
             const float *cw = comb_w + t * (K + 1), *cg = comb_g + t * (K + 1);
-            float acc = __bfloat162float(p.x[(size_t)t * H + h]);
             float y = 0.0f;
             int lq = 0, lk = 0;  // (slot, chunk) of the next term to load
             int aq = 0, ak = 0;  // ... and to add
@@ -1075,21 +1108,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
-    }
-    if (tid == 0) {
-        __threadfence();
-        if (atom_add_acq_rel_gpu(&p.hdr->exit_cnt, 1u) == gridDim.x - 1) {
-            // every CTA is done with the counters: leave them zero for the next launch
-            for (int i = 0; i < pair_prefix[G]; ++i) {
-                p.group_ready[i] = 0;
-                p.x_ready[i] = 0;
-            }
-            for (int i = 0; i < H / 256; ++i) p.htile_cnt[i] = 0;
-            p.hdr->job_next = 0;
-            __threadfence();
-            p.hdr->exit_cnt = 0;
-            __threadfence();
-        }
     }
 }
 

@@ -39,13 +39,17 @@ struct WeightsDev {
 };
 
 // Workspace header, at the start of the caller's workspace (256 B).
+// The tensor-core path keeps two sets of its launch-wide counters and uses
+// them in alternate launches: a launch finds its own set zeroed by the launch
+// before it and zeroes the other set, so no CTA has to reset anything at exit.
 struct WsHeader {
-    uint32_t err;        // device error word (MOE_DEV_* bits)
-    uint32_t bar_count;  // grid barrier: arrivals in the current round
-    uint32_t bar_gen;    // grid barrier: completed rounds (monotonic)
-    uint32_t job_next;   // tensor-core path: next job to claim
-    uint32_t exit_cnt;   // tensor-core path: CTAs finished
-    uint32_t pad[59];
+    uint32_t err;          // device error word (MOE_DEV_* bits)
+    uint32_t bar_count;    // grid barrier: arrivals in the current round
+    uint32_t bar_gen;      // grid barrier: completed rounds (monotonic)
+    uint32_t start_cnt;    // tensor-core path: CTA starts modulo 2*grid; start_cnt / grid = launch parity
+    uint32_t job_next[2];  // tensor-core path, per parity: jobs claimed past the first round
+    uint32_t x_ready[2];   // tensor-core path, per parity: CTAs done converting their activation slice
+    uint32_t pad[56];
 };
 static_assert(sizeof(WsHeader) == 256, "header size");
 

@@ -126,6 +126,19 @@ __device__ __forceinline__ void tma_load_3d_hint(void *dst, const void *tmap, in
         : "memory");
 }
 
+// Named CTA barrier `id` (1..15; 0 is __syncthreads) over `nthreads` threads,
+// a multiple of 32.
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// 16-byte asynchronous copy that reads src_bytes (0 or 16) bytes of src and
+// zero-fills the rest: with 0 nothing is read.
+__device__ __forceinline__ void cp_async16_zfill(void *dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+
 // 16-byte asynchronous copy global (L2) -> shared, outside the TMA unit.
 __device__ __forceinline__ void cp_async16(void *dst, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
