@@ -35,6 +35,8 @@ moe_status cuda_fail(cudaError_t e, const char *what) {
 constexpr int kMaxT = 256, kMaxK = 16, kMaxE = 1024, kMaxDim = 16384;
 static_assert(kMaxT * (kMaxK + 1) <= moe::kTcReadyCap, "group_ready capacity");
 static_assert(kMaxDim / 256 <= moe::kTcHtileCap, "htile_cnt capacity");
+static_assert(moe::group_table_scratch_ints(kMaxT, kMaxK, kMaxE) * 4 <= moe::kRawStageBytes,
+              "the group table scratch fits in one raw stage");
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 

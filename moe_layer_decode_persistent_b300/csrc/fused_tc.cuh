@@ -282,6 +282,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
     // other warps convert the activations meanwhile, then fill the combine
     // coefficients, then take up their roles.
     const int nw1 = kTcThreads - 32;  // threads of warps 1..
+    // one raw stage: tile0 and tile1 boxes of 128 bytes x 128 rows at byte
+    // column kb (and their NVFP4 scale boxes at column ks), completing on rfull
+    auto tma_stage = [&](int st, const CUtensorMap *mc, const CUtensorMap *ms, bool fp4, int kb, int ks, int rows0,
+                         int rows1, int e, uint64_t pol) {
+        uint8_t *dst = raw + st * kRawStageBytes;
+        mbar_arrive_expect_tx(&rfull[st], fp4 ? kRawStageBytes : 2 * kRawTileBytes);
+        tma_load_3d_hint(dst, mc, kb, rows0, e, &rfull[st], pol);
+        tma_load_3d_hint(dst + kRawTileBytes, mc, kb, rows1, e, &rfull[st], pol);
+        if (fp4) {
+            tma_load_3d_hint(dst + kRawScaleOff, ms, ks, rows0, e, &rfull[st], pol);
+            tma_load_3d_hint(dst + kRawScaleOff + 2048, ms, ks, rows1, e, &rfull[st], pol);
+        }
+    };
+    int npre = 0;  // stages of this CTA's first job issued before the group table
     if (warp == 0 && lane == 0) {
         for (int i = 0; i < kJobSlots; ++i) {
             mbar_init(&jfull[i], 1);
@@ -303,6 +317,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
         for (int i = 0; i < 64; ++i) tile_ready_s[i] = 0;
         *abort_flag = 0;
         fence_mbar_init();
+        // The shared expert is group 0 in either form and its gate/up jobs come
+        // first in the list, so when this CTA's first job (job b) is one of them
+        // the shape alone defines it: its first stages stream in while the group
+        // table is built (the table's scratch sits in the ring's last stage).
+        const int fmt0 = p.shared.fmt, nt0 = tc_nt(fmt0, T), n0 = no_dedup ? 1 : T;
+        const int tiles0 = p.Is / 128, nkc0 = tc_nkc_gu(fmt0, H, T), b = (int)blockIdx.x;
+        if (b < ((n0 + nt0 - 1) / nt0) * tiles0 * nkc0) {
+            fence_proxy_async_smem();
+            const int rem = b % (tiles0 * nkc0), tile = rem / nkc0, kc = rem - (rem / nkc0) * nkc0;
+            const int kc_len = tc_kc_gu(fmt0, H, T), k0 = kc * kc_len;
+            const bool fp4 = fmt0 == kFmtNvfp4;
+            const int nst = (min(kc_len, H - k0) / kUnitK) / (fp4 ? 2 : 1);
+            npre = min(nst, nR - 1);
+            const uint64_t pol = l2_evict_first_policy();
+            for (int st = 0; st < npre; ++st)
+                tma_stage(st, &p.maps.s13, &p.maps.s13s, fp4, (fp4 ? k0 / 2 : k0) + st * 128, k0 / 16 + st * 16,
+                          tile * 128, p.Is + tile * 128, 0, pol);
+        }
     }
     uint32_t start_no = 0;
     if (warp == 1) {
@@ -315,9 +347,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
     if (warp >= 1) tc_convert_x(p, (tid - 32) * (int)gridDim.x + (int)blockIdx.x, nw1 * (int)gridDim.x);
     if (tid == 32) *par_s = (int)(start_no / gridDim.x);
 
-    // group table (its scratch aliases the raw ring; it ends with a CTA barrier,
-    // which also publishes the barriers, the parity and the TMEM address)
-    group_table_cta(p.ids, T, K, p.E, no_dedup, tab, reinterpret_cast<int *>(raw),
+    // group table (its scratch is the raw ring's last stage; it ends with a CTA
+    // barrier, which also publishes the barriers, the parity and the TMEM address)
+    group_table_cta(p.ids, T, K, p.E, no_dedup, tab, reinterpret_cast<int *>(raw + (nR - 1) * kRawStageBytes),
                     blockIdx.x == 0 ? err : nullptr);
     const int G = tab.G();
     const int32_t *gexp = tab.gexp(), *gn = tab.gncols(), *g0 = tab.gcol0(), *rcol = tab.row_col();
@@ -428,9 +460,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
         // ===================== producer =====================
         if (lane == 0) {
             const int NGU = gu_prefix[G], njobs = NGU + dn_prefix[G];
-            int js = 0, jph = 0, rs = 0, rph = 0;
+            int js = 0, jph = 0, rs = npre, rph = 0;  // npre < nR
             int cur_gu = 0, cur_dn = 0;
-            uint32_t armed = 0;  // raw stages with a TMA in flight not yet seen consumed
+            int skip = npre;                         // the first job's stages already issued
+            uint32_t armed = (1u << npre) - 1u;     // raw stages with a TMA in flight not yet seen consumed
             // CTA b takes job b first, with no claim; later jobs come from the counter
             int j = (int)blockIdx.x;
             for (;; j = (int)gridDim.x + (int)atomicAdd(&p.hdr->job_next[par], 1u)) {
@@ -515,27 +548,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                 const int kb0 = fp4 ? d.k0 / 2 : d.k0;
                 const uint64_t pol = l2_evict_first_policy();  // weights are read once
                 bool ok = true;
-                for (int s = 0; s < nst; ++s) {
+                for (int s = skip; s < nst; ++s) {
                     if (!mbar_wait(&rempty[rs], rph ^ 1, abort_flag, err)) {
                         ok = false;
                         break;
                     }
                     armed &= ~(1u << rs);
-                    uint8_t *dst = raw + rs * kRawStageBytes;
-                    mbar_arrive_expect_tx(&rfull[rs], fp4 ? kRawStageBytes : 2 * kRawTileBytes);
-                    tma_load_3d_hint(dst, mc, kb0 + s * 128, d.rows0, d.e, &rfull[rs], pol);
-                    tma_load_3d_hint(dst + kRawTileBytes, mc, kb0 + s * 128, d.rows1, d.e, &rfull[rs], pol);
-                    if (fp4) {
-                        tma_load_3d_hint(dst + kRawScaleOff, ms, d.k0 / 16 + s * 16, d.rows0, d.e, &rfull[rs], pol);
-                        tma_load_3d_hint(dst + kRawScaleOff + 2048, ms, d.k0 / 16 + s * 16, d.rows1, d.e,
-                                         &rfull[rs], pol);
-                    }
+                    tma_stage(rs, mc, ms, fp4, kb0 + s * 128, d.k0 / 16 + s * 16, d.rows0, d.rows1, d.e, pol);
                     armed |= 1u << rs;
                     if (++rs == nR) {
                         rs = 0;
                         rph ^= 1;
                     }
                 }
+                skip = 0;
                 if (!ok) break;
             }
             // never leave with a TMA write into shared memory still in flight
