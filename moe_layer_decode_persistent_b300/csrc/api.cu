@@ -78,15 +78,17 @@ WsLayout ws_layout(const moe_shape *s) {
     L.fma_end = align_up(off, 256);
 
     off = L.tc_ctrl_end;
-    const int Ti = (int)T, Hi = (int)H;
-    const size_t nkc_gu = Ti <= moe::kSplitMaxT
-                              ? (size_t)std::max(moe::tc_nkc_gu(moe::kFmtNvfp4, Hi, Ti),
-                                                 moe::tc_nkc_gu(moe::kFmtFp8B128, Hi, Ti))
-                              : 0;
+    // The K-chunk partials are sized for the most chunks any T' <= T uses (one
+    // row, the shortest jobs, at up to kSplitMaxT rows), so the size for T also
+    // serves every smaller T.
+    const int Hi = (int)H;
+    const size_t Tsplit = std::min(T, (size_t)moe::kSplitMaxT), Usplit = Tsplit * (K + 1);
+    const size_t nkc_gu = (size_t)std::max(moe::tc_nkc_gu(moe::kFmtNvfp4, Hi, 1), moe::tc_nkc_gu(moe::kFmtFp8B128, Hi, 1));
+    const size_t y_cols = std::max((size_t)moe::tc_nkc_dn((int)Imax, 1) * Usplit, Ucap);
     L.tc_P = off;
-    off += nkc_gu * 2 * Ucap * Imax * sizeof(float);
+    off += nkc_gu * 2 * Usplit * Imax * sizeof(float);
     L.tc_Y = off = align_up(off, 256);
-    off += (size_t)moe::tc_nkc_dn((int)Imax, Ti) * Ucap * H * sizeof(float);
+    off += y_cols * H * sizeof(float);
     // sum over (group, column tile) of the padded column counts: each group pads
     // its last column tile to a multiple of 16, so it is at most U + 15 * G <=
     // 16 * U in either form (the size does not depend on the flags)

@@ -136,18 +136,27 @@ struct TcJob {
 
 // ---- per-launch constants shared by host and device -----------------------
 
+// K chunks of the jobs up to kSplitMaxT rows. A launch with more rows streams
+// more distinct experts per CTA, so its jobs are made twice as long: every job
+// boundary costs a hand-off, while the last jobs' length sets how far apart the
+// CTAs finish, which matters most when there are few jobs per CTA. The chunks
+// depend on the launch's shape alone, never on its groups.
+constexpr int kShortJobsMaxT = 2;
+__host__ __device__ inline int tc_kc_gu(int fmt, int H, int T) {
+    if (T > kSplitMaxT) return H;
+    return (fmt == kFmtNvfp4 ? kKcNvfp4 : kKcFp8) * (T > kShortJobsMaxT ? 2 : 1);
+}
 __host__ __device__ inline int tc_nkc_gu(int fmt, int H, int T) {
-    if (T > kSplitMaxT) return 1;
-    const int kc = fmt == kFmtNvfp4 ? kKcNvfp4 : kKcFp8;
+    const int kc = tc_kc_gu(fmt, H, T);
     return (H + kc - 1) / kc;
 }
-__host__ __device__ inline int tc_kc_gu(int fmt, int H, int T) {
-    return T > kSplitMaxT ? H : (fmt == kFmtNvfp4 ? kKcNvfp4 : kKcFp8);
+__host__ __device__ inline int tc_kc_dn(int Ig, int T) {
+    return T > kSplitMaxT ? Ig : kKcDown * (T > kShortJobsMaxT ? 2 : 1);
 }
 __host__ __device__ inline int tc_nkc_dn(int Ig, int T) {
-    return T > kSplitMaxT ? 1 : (Ig + kKcDown - 1) / kKcDown;
+    const int kc = tc_kc_dn(Ig, T);
+    return (Ig + kc - 1) / kc;
 }
-__host__ __device__ inline int tc_kc_dn(int Ig, int T) { return T > kSplitMaxT ? Ig : kKcDown; }
 
 // B-operand layout of a [n][128] f16 unit: core matrices of 8 columns x 8 K.
 __device__ __forceinline__ uint32_t b_off(int n, int k) {
