@@ -44,7 +44,7 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 // and the tensor path's counters come next in a region the CUDA-core path never
 // writes, so they stay valid when the two paths take turns on one workspace:
 //   header | group_ready [2][kTcReadyCap] | htile_cnt [2][kTcHtileCap] |
-//   tile_cnt [C*Imax/128*4] | then
+//   tile_cnt [16*(K+1)*Imax/128*4] | then
 //   CUDA-core path : mid fp32 [Ucap][Imax] | y fp32 [Ucap][H]
 //   tensor path    : P | Y | midB | xh f16 [T][H]
 // followed by the host-buffer call's staging area. Ucap = C = T*(K+1).
@@ -67,8 +67,11 @@ WsLayout ws_layout(const moe_shape *s) {
     off += 2 * (size_t)moe::kTcReadyCap * 4;
     L.tc_htile = off = align_up(off, 16);
     off += 2 * (size_t)moe::kTcHtileCap * 4;
+    // tile_cnt is used up to kSplitMaxT rows and sized for that many whatever T
+    // is, so the counter region does not move or grow with T: a CUDA-core launch
+    // with a smaller T never writes over a larger T's counters
     L.tc_tile = off = align_up(off, 16);
-    off += Ucap * (Imax / 128) * 4 * 4;
+    off += (size_t)moe::kSplitMaxT * (K + 1) * (Imax / 128) * 4 * 4;
     L.tc_ctrl_end = off = align_up(off, 256);
 
     L.mid = off;

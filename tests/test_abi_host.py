@@ -51,6 +51,17 @@ def test_workspace_bytes_grow_with_T_and_reject_bad_shapes():
         assert B.moe_workspace_bytes(_shape(**bad)) == 0, bad
 
 
+def test_workspace_bytes_never_shrink_as_T_grows():
+    # the header states that a workspace sized for T serves every smaller T;
+    # the tensor path's K-chunk partials change shape at T=3 and T=17
+    for dims in (dict(H=7168, I=2048, I_shared=2048, E=256, K=8), dict(H=512, I=256, I_shared=512, E=16, K=4)):
+        prev = 0
+        for T in range(0, 257):
+            n = B.moe_workspace_bytes(_shape(T=T, **dims))
+            assert n >= prev, (dims, T, n, prev)
+            prev = n
+
+
 def test_group_table_ints():
     assert B.moe_group_table_ints(4, 2) == 2 + 5 * 4 * 3
     assert B.moe_group_table_ints(0, 8) == 2

@@ -127,6 +127,22 @@ def test_repeat_launches_are_identical(path):
         assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
+def test_paths_and_shapes_take_turns_on_one_workspace():
+    # The tensor-core kernel keeps launch-wide counters in two sets used by
+    # alternate launches, in a region the CUDA-core kernel never writes; a
+    # workspace sized for T=8 also serves T=1. Interleave all of it on one
+    # workspace and compare with fresh workspaces, bit for bit.
+    L8 = layer(inputs.dsv3(8), "mtp", seed=5)
+    L1 = layer(inputs.dsv3(1), "uniform", seed=6)
+    ws = workspace(L8)
+    ref = {(n, p): run_fused(L, PATHS[p]) for n, L in (("t8", L8), ("t1", L1)) for p in ("mma", "fma")}
+    order = [("t8", "mma"), ("t8", "fma"), ("t8", "mma"), ("t1", "mma"), ("t1", "fma"), ("t8", "mma"),
+             ("t1", "mma"), ("t1", "mma"), ("t8", "fma"), ("t8", "mma")]
+    for n, p in order:
+        out = run_fused(L8 if n == "t8" else L1, PATHS[p], ws=ws)
+        assert torch.equal(out.view(torch.int16), ref[(n, p)].view(torch.int16)), (n, p)
+
+
 @pytest.mark.parametrize("path", list(PATHS))
 def test_duplicate_rows_and_permutation(path):
     s = inputs.Shape(T=9, H=512, I=256, I_shared=512, E=16, K=4)
