@@ -10,19 +10,25 @@
 // CTAs; a row's output is summed in a fixed order so the dedup form is bitwise
 // equal to the one-row form).
 //
-// Work items ("jobs"), claimed in list order from one global counter:
+// Work items ("jobs"); CTA b takes job b first, later jobs are claimed in list
+// order from one global counter:
 //   gate/up job (group g, column tile ct, 128-row tile rt, K chunk kc):
 //     tile0 = gate rows rt*128.., tile1 = up rows I+rt*128.., K = H chunk
 //   down job (g, ct, 256-row tile ht, K chunk kc):
 //     tile0 = rows ht*256.., tile1 = rows ht*256+128.., K = I chunk
 // Both tiles of a job share the B operand (the group's activation columns).
+// The K chunks depend on the launch's shape only (the dedup and one-row forms
+// split work alike). The launch-wide counters (job claims, ready counts) come
+// in two sets that alternate by launch parity, each launch zeroing the other.
 //
 // Per CTA the roles are warp-specialised (18 warps; 26 with the two-parity
 // dequant build option):
 //   warp 0      producer: claims jobs, TMA-loads 128-byte-wide weight boxes
 //               (SWIZZLE_128B) and NVFP4 block scales into a ring of 2 to 6
-//               stages (as many as shared memory holds next to the tables);
-//               at the end it watches the output tiles for the combine
+//               stages (as many as shared memory holds next to the tables),
+//               the first ones before the group table is built where the
+//               shape alone defines the first job; at the end it watches the
+//               output tiles for the combine
 //   warp 1      B stager: copies the job's B tile per 128-K unit with
 //               cp.async (not the TMA queue, which is full of weight boxes):
 //               gate/up gathers each column from its row of the f16
