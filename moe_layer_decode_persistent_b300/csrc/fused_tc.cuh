@@ -479,9 +479,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
             int cur_gu = 0, cur_dn = 0;
             int skip = npre;                         // the first job's stages already issued
             uint32_t armed = (1u << npre) - 1u;     // raw stages with a TMA in flight not yet seen consumed
-            // CTA b takes job b first, with no claim; later jobs come from the counter
+            // CTA b takes job b first, with no claim; later jobs come from the counter.
+            // The next job is claimed just before the current job's last stage
+            // waits for its slot, so the claim's round trip overlaps that wait.
             int j = (int)blockIdx.x;
-            for (;; j = (int)gridDim.x + (int)atomicAdd(&p.hdr->job_next[par], 1u)) {
+            for (;;) {
                 TcJob d;
                 if (*abort_flag || j >= njobs) {
                     d.kind = -1;
@@ -563,7 +565,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                 const int kb0 = fp4 ? d.k0 / 2 : d.k0;
                 const uint64_t pol = l2_evict_first_policy();  // weights are read once
                 bool ok = true;
+                int next = -1;
                 for (int s = skip; s < nst; ++s) {
+                    if (s == nst - 1) next = (int)gridDim.x + (int)atomicAdd(&p.hdr->job_next[par], 1u);
                     if (!mbar_wait(&rempty[rs], rph ^ 1, abort_flag, err)) {
                         ok = false;
                         break;
@@ -578,6 +582,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                 }
                 skip = 0;
                 if (!ok) break;
+                j = next >= 0 ? next : (int)gridDim.x + (int)atomicAdd(&p.hdr->job_next[par], 1u);
             }
             // never leave with a TMA write into shared memory still in flight
             if (*abort_flag && armed) {
