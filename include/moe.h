@@ -201,9 +201,10 @@ moe_status moe_fused_decode_host(const void *x_host, const int32_t *ids_host,
  * intermediates are the smaller scratch): the scratch is a file-scope device
  * array of 8 MiB inside the library, which
  * every GPU that loads the library holds until the process exits. Shapes
- * whose CUDA-core scratch, 256 + 4*T*(K+1)*(max(I, I_shared) + H) bytes,
- * exceeds 8 MiB are rejected with MOE_ERR_WORKSPACE before anything is
- * launched (DeepSeek-V3 shapes: T <= 24).
+ * whose CUDA-core scratch, about 36 KB + 2*(K+1)*Imax +
+ * 4*T*(K+1)*(Imax + H) bytes with Imax = max(I, I_shared), exceeds 8 MiB are
+ * rejected with MOE_ERR_WORKSPACE before anything is launched (DeepSeek-V3
+ * shapes: T <= 25).
  *   err_out  optional device uint32: receives the call's device error word
  *            (MOE_DEV_* bits); NULL to ignore it.
  * The first call on a device looks up the array's device address there (with
