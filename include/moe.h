@@ -118,7 +118,10 @@ typedef struct {
 
 /* Bytes of device workspace moe_fused_decode needs for this shape (the
  * error word, inter-CTA counters and the fp32 intermediates). Sizes for a
- * larger T also serve any smaller T with the same other fields. */
+ * larger T also serve any smaller T with the same other fields. One
+ * workspace may serve launches of different shapes (T, K, I, I_shared) as
+ * long as it is at least moe_workspace_bytes of each: the counters sit at
+ * the same offsets for every shape. */
 size_t moe_workspace_bytes(const moe_shape *s);
 
 /* Zero a workspace (async on stream). Required once before first use and
@@ -201,14 +204,17 @@ moe_status moe_fused_decode_host(const void *x_host, const int32_t *ids_host,
  * intermediates are the smaller scratch): the scratch is a file-scope device
  * array of 8 MiB inside the library, which
  * every GPU that loads the library holds until the process exits. Shapes
- * whose CUDA-core scratch, about 36 KB + 2*(K+1)*Imax +
- * 4*T*(K+1)*(Imax + H) bytes with Imax = max(I, I_shared), exceeds 8 MiB are
+ * whose CUDA-core scratch, 256 + 4*T*(K+1)*(Imax + H) bytes (rounded up to
+ * 256-byte boundaries) with Imax = max(I, I_shared), exceeds 8 MiB are
  * rejected with MOE_ERR_WORKSPACE before anything is launched (DeepSeek-V3
  * shapes: T <= 25).
  *   err_out  optional device uint32: receives the call's device error word
  *            (MOE_DEV_* bits); NULL to ignore it.
- * The first call on a device looks up the array's device address there (with
- * that device current); make that first call before any stream capture.
+ * The first call in a CUDA context looks up the array's device address there
+ * (with that context's device current) and keeps it under the context's
+ * unique id, so a context created later (another driver-API context, or the
+ * runtime's after cudaDeviceReset) gets its own lookup; make the first call
+ * in each context before any stream capture.
  * All calls share the one array and it keeps the last call's contents; each
  * call leaves its header cleared for the next. Calls that overlap on the GPU
  * (different streams, or threads) race on it: serialise them. This entry

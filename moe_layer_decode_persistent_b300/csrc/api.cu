@@ -6,9 +6,10 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <string>
-#include <unordered_map>
+#include <vector>
 
 #include "../../include/moe.h"
 #include "fused_fma.cuh"
@@ -44,10 +45,15 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 // and the tensor path's counters come next in a region the CUDA-core path never
 // writes, so they stay valid when the two paths take turns on one workspace:
 //   header | group_ready [2][kTcReadyCap] | htile_cnt [2][kTcHtileCap] |
-//   tile_cnt [16*(K+1)*Imax/128*4] | then
+//   tile_cnt [kTcTileCntWords] | then
 //   CUDA-core path : mid fp32 [Ucap][Imax] | y fp32 [Ucap][H]
 //   tensor path    : P | Y | midB | xh f16 [T][H]
-// followed by the host-buffer call's staging area. Ucap = C = T*(K+1).
+// followed by the host-buffer call's staging area. Ucap = C = T*(K+1). The
+// counter region's size is a constant (sized from the largest T, K and
+// intermediate the tensor path splits), so it sits at the same offsets for
+// every shape: launches of different T, K, I or I_shared on one workspace
+// never find their counters under another shape's scratch.
+constexpr size_t kTcTileCntWords = (size_t)moe::kSplitMaxT * (kMaxK + 1) * (kMaxDim / 128) * 4;
 struct WsLayout {
     size_t mid = 0, y = 0, fma_end = 0;
     size_t tc_ready = 0, tc_htile = 0, tc_tile = 0, tc_ctrl_end = 0, tc_P = 0, tc_Y = 0, tc_midB = 0,
@@ -67,11 +73,11 @@ WsLayout ws_layout(const moe_shape *s) {
     off += 2 * (size_t)moe::kTcReadyCap * 4;
     L.tc_htile = off = align_up(off, 16);
     off += 2 * (size_t)moe::kTcHtileCap * 4;
-    // tile_cnt is used up to kSplitMaxT rows and sized for that many whatever T
-    // is, so the counter region does not move or grow with T: a CUDA-core launch
-    // with a smaller T never writes over a larger T's counters
+    // tile_cnt: one word per (group, column tile, 128-row tile, quarter) of a
+    // launch that splits K, i.e. at most kSplitMaxT*(K+1) column tiles times
+    // Imax/128 row tiles; sized for the caps so the region never moves
     L.tc_tile = off = align_up(off, 16);
-    off += (size_t)moe::kSplitMaxT * (K + 1) * (Imax / 128) * 4 * 4;
+    off += kTcTileCntWords * 4;
     L.tc_ctrl_end = off = align_up(off, 256);
 
     L.mid = off;
@@ -182,18 +188,29 @@ struct DevInfo {
     int tc_static_smem = 0;  // static shared memory of the tensor-core kernel
 };
 
+// Per-device facts, filled once per device (under a lock) and read without one.
+constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-std::unordered_map<int, DevInfo> g_dev;
+DevInfo g_dev[kMaxDevices];
+std::atomic<bool> g_dev_ready[kMaxDevices];
 
-moe_status dev_info(DevInfo *out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+moe_status current_device(int *dev) {
+    cudaError_t e = cudaGetDevice(dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (*dev < 0 || *dev >= kMaxDevices)
+        return fail(MOE_ERR_UNSUPPORTED, "device %d: the library handles devices 0..%d", *dev, kMaxDevices - 1);
+    return MOE_OK;
+}
+
+moe_status dev_info(int dev, DevInfo *out) {
+    if (g_dev_ready[dev].load(std::memory_order_acquire)) {
+        *out = g_dev[dev];
+        return MOE_OK;
+    }
     std::lock_guard<std::mutex> lk(g_mu);
-    auto it = g_dev.find(dev);
-    if (it == g_dev.end()) {
+    if (!g_dev_ready[dev].load(std::memory_order_relaxed)) {
         DevInfo d;
-        e = cudaDeviceGetAttribute(&d.nsm, cudaDevAttrMultiProcessorCount, dev);
+        cudaError_t e = cudaDeviceGetAttribute(&d.nsm, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
         e = cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
         if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(smem)");
@@ -201,9 +218,10 @@ moe_status dev_info(DevInfo *out) {
         e = cudaFuncGetAttributes(&fa, moe::fused_tc_kernel<false>);
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncGetAttributes");
         d.tc_static_smem = (int)fa.sharedSizeBytes;
-        it = g_dev.emplace(dev, d).first;
+        g_dev[dev] = d;
+        g_dev_ready[dev].store(true, std::memory_order_release);
     }
-    *out = it->second;
+    *out = g_dev[dev];
     return MOE_OK;
 }
 
@@ -224,46 +242,45 @@ moe_status set_smem(Kern k, size_t smem, const DevInfo &d) {
 }
 
 // Blocks per SM of a kernel at a dynamic smem size, with the smem attribute
-// set; cached per (device, kernel, smem) so a launch inside stream capture
-// makes no other CUDA call.
+// set; cached per (device, kernel, threads, smem) so a launch inside stream
+// capture makes no other CUDA call.
 template <typename Kern>
-moe_status plan_occupancy(Kern k, int threads, size_t smem, const DevInfo &d, int *occ_out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+moe_status plan_occupancy(Kern k, int dev, int threads, size_t smem, const DevInfo &d, int *occ_out) {
+    struct Entry {
+        int dev;
+        const void *k;
+        int threads;
+        size_t smem;
+        int occ;
+    };
     static std::mutex mu;
-    static std::unordered_map<std::string, int> cache;
-    char key[128];
-    snprintf(key, sizeof key, "%d/%p/%d/%zu", dev, (const void *)k, threads, smem);
+    static std::vector<Entry> cache;
     {
         std::lock_guard<std::mutex> lk(mu);
-        auto it = cache.find(key);
-        if (it != cache.end()) {
-            *occ_out = it->second;
-            return MOE_OK;
-        }
+        for (const Entry &c : cache)
+            if (c.dev == dev && c.k == (const void *)k && c.threads == threads && c.smem == smem) {
+                *occ_out = c.occ;
+                return MOE_OK;
+            }
     }
     moe_status st = set_smem(k, smem, d);
     if (st != MOE_OK) return st;
     int occ = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, threads, smem);
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, threads, smem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
     if (occ < 1) return fail(MOE_ERR_UNSUPPORTED, "kernel does not fit on an SM (%zu B smem)", smem);
     std::lock_guard<std::mutex> lk(mu);
-    cache[key] = occ;
+    cache.push_back({dev, (const void *)k, threads, smem, occ});
     *occ_out = occ;
     return MOE_OK;
 }
 
-moe_status launch_fused_fma(const moe::FusedParams &p, const moe_shape *s, cudaStream_t stream) {
-    DevInfo d;
-    moe_status st = dev_info(&d);
-    if (st != MOE_OK) return st;
+moe_status launch_fused_fma(const moe::FusedParams &p, const moe_shape *s, int dev, const DevInfo &d,
+                            cudaStream_t stream) {
     const size_t smem = table_smem_bytes(s);
     int occ = 0;
-    st = plan_occupancy(moe::fused_fma_kernel, moe::kFmaThreads, smem, d, &occ);
+    moe_status st = plan_occupancy(moe::fused_fma_kernel, dev, moe::kFmaThreads, smem, d, &occ);
     if (st != MOE_OK) return st;
-    cudaError_t e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(d.nsm * occ));
     cfg.blockDim = dim3(moe::kFmaThreads);
@@ -274,7 +291,7 @@ moe_status launch_fused_fma(const moe::FusedParams &p, const moe_shape *s, cudaS
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, moe::fused_fma_kernel, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, moe::fused_fma_kernel, p);
     if (e != cudaSuccess) return cuda_fail(e, "launch fused_fma_kernel");
     return MOE_OK;
 }
@@ -306,31 +323,6 @@ moe_status encode_fn(EncodeTiledFn *out) {
 // 3-D uint8 map over [E][rows][cols] bytes; box [box_c][128][1].
 moe_status tensor_map(CUtensorMap *out, const void *base, size_t cols, size_t rows, size_t E, int box_c,
                       bool swz128) {
-    struct Key {
-        const void *b;
-        size_t c, r, e;
-        int bc, sw;
-        bool operator==(const Key &o) const {
-            return b == o.b && c == o.c && r == o.r && e == o.e && bc == o.bc && sw == o.sw;
-        }
-    };
-    struct KeyHash {
-        size_t operator()(const Key &k) const {
-            return std::hash<const void *>()(k.b) ^ (k.c * 1000003u) ^ (k.r * 10007u) ^ (k.e * 101u) ^
-                   (size_t)k.bc ^ ((size_t)k.sw << 20);
-        }
-    };
-    static std::mutex mu;
-    static std::unordered_map<Key, CUtensorMap, KeyHash> cache;
-    const Key key{base, cols, rows, E, box_c, swz128 ? 1 : 0};
-    {
-        std::lock_guard<std::mutex> lk(mu);
-        auto it = cache.find(key);
-        if (it != cache.end()) {
-            *out = it->second;
-            return MOE_OK;
-        }
-    }
     EncodeTiledFn enc;
     moe_status st = encode_fn(&enc);
     if (st != MOE_OK) return st;
@@ -343,8 +335,6 @@ moe_status tensor_map(CUtensorMap *out, const void *base, size_t cols, size_t ro
                      swz128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
-    std::lock_guard<std::mutex> lk(mu);
-    cache[key] = *out;
     return MOE_OK;
 }
 
@@ -366,8 +356,63 @@ moe_status set_maps(const moe_weights *w, int E, int H, int I, CUtensorMap *m13,
     return MOE_OK;
 }
 
+// The eight tensor maps of a (routed, shared, shape) triple, cached: encoding
+// them costs microseconds of host time, and a caller typically cycles over a
+// few resident weight sets (one per layer). Up to kMapsCache entries, replaced
+// in turn.
+moe_status tc_maps(const moe_weights *routed, const moe_weights *shared, const moe_shape *s, moe::TcMaps *out) {
+    struct Key {
+        const void *p[8];
+        int fr, fs, E, H, I, Is;
+        bool operator==(const Key &o) const { return memcmp(this, &o, sizeof(Key)) == 0; }
+    };
+    struct Entry {
+        Key k;
+        moe::TcMaps m;
+    };
+    constexpr int kMapsCache = 32;
+    static std::mutex mu;
+    static Entry cache[kMapsCache];
+    static int used = 0, next = 0;
+    Key key;
+    memset(&key, 0, sizeof key);
+    key.p[0] = routed->w13;
+    key.p[1] = routed->w13_scale;
+    key.p[2] = routed->w2;
+    key.p[3] = routed->w2_scale;
+    key.p[4] = shared->w13;
+    key.p[5] = shared->w13_scale;
+    key.p[6] = shared->w2;
+    key.p[7] = shared->w2_scale;
+    key.fr = routed->fmt;
+    key.fs = shared->fmt;
+    key.E = s->E;
+    key.H = s->H;
+    key.I = s->I;
+    key.Is = s->I_shared;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        for (int i = 0; i < used; ++i)
+            if (cache[i].k == key) {
+                *out = cache[i].m;
+                return MOE_OK;
+            }
+    }
+    moe::TcMaps m;
+    moe_status st = set_maps(routed, s->E, s->H, s->I, &m.r13, &m.r13s, &m.r2, &m.r2s);
+    if (st == MOE_OK) st = set_maps(shared, 1, s->H, s->I_shared, &m.s13, &m.s13s, &m.s2, &m.s2s);
+    if (st != MOE_OK) return st;
+    std::lock_guard<std::mutex> lk(mu);
+    const int slot = used < kMapsCache ? used++ : (next++ % kMapsCache);
+    cache[slot].k = key;
+    cache[slot].m = m;
+    *out = m;
+    return MOE_OK;
+}
+
 // Whether the tensor-core path handles this launch (and why not).
-bool tc_eligible(const moe_shape *s, const moe_weights *routed, const moe_weights *shared, const char **why) {
+bool tc_eligible(const moe_shape *s, const moe_weights *routed, const moe_weights *shared, const DevInfo &d,
+                 const char **why) {
     if (routed->fmt == MOE_W_BF16 || shared->fmt == MOE_W_BF16) {
         *why = "bf16 weights use the CUDA-core path";
         return false;
@@ -380,11 +425,6 @@ bool tc_eligible(const moe_shape *s, const moe_weights *routed, const moe_weight
         *why = "T above 256";
         return false;
     }
-    DevInfo d;
-    if (dev_info(&d) != MOE_OK) {
-        *why = "device query failed";
-        return false;
-    }
     const bool nd = (s->flags & MOE_FLAG_NO_DEDUP) != 0;
     if (moe::tc_smem_bytes(s->T, s->K, s->E, nd, moe::kRawStagesMin) > d.max_smem_optin - d.tc_static_smem) {
         *why = "group tables do not fit in shared memory";
@@ -394,17 +434,12 @@ bool tc_eligible(const moe_shape *s, const moe_weights *routed, const moe_weight
 }
 
 moe_status launch_fused_tc(const moe::FusedParams &fp, const WsLayout &L, const moe_shape *s,
-                           const moe_weights *routed, const moe_weights *shared, cudaStream_t stream) {
-    DevInfo d;
-    moe_status st = dev_info(&d);
-    if (st != MOE_OK) return st;
+                           const moe_weights *routed, const moe_weights *shared, int dev, const DevInfo &d,
+                           cudaStream_t stream) {
     moe::TcParams p;
     memset(&p, 0, sizeof p);
-    if ((st = set_maps(routed, s->E, s->H, s->I, &p.maps.r13, &p.maps.r13s, &p.maps.r2, &p.maps.r2s)) != MOE_OK)
-        return st;
-    if ((st = set_maps(shared, 1, s->H, s->I_shared, &p.maps.s13, &p.maps.s13s, &p.maps.s2, &p.maps.s2s)) !=
-        MOE_OK)
-        return st;
+    moe_status st = tc_maps(routed, shared, s, &p.maps);
+    if (st != MOE_OK) return st;
     p.x = fp.x;
     p.ids = fp.ids;
     p.topk_w = fp.topk_w;
@@ -439,7 +474,7 @@ moe_status launch_fused_tc(const moe::FusedParams &fp, const WsLayout &L, const 
     int occ = 0;
     const bool capped = moe::tc_capped_tables(s->T);
     auto kern = capped ? moe::fused_tc_kernel<true> : moe::fused_tc_kernel<false>;
-    if ((st = plan_occupancy(kern, moe::kTcThreads, smem, d, &occ)) != MOE_OK) return st;
+    if ((st = plan_occupancy(kern, dev, moe::kTcThreads, smem, d, &occ)) != MOE_OK) return st;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)d.nsm);  // one CTA per SM: it holds all of TMEM
     cfg.blockDim = dim3(moe::kTcThreads);
@@ -455,24 +490,38 @@ moe_status launch_fused_tc(const moe::FusedParams &fp, const WsLayout &L, const 
     return MOE_OK;
 }
 
+// CUDA-core scratch laid out straight after the header (no tensor-path
+// counter region): for a scratch buffer that only the CUDA-core kernel ever
+// uses. Returns its size; mid and y get their offsets.
+size_t fma_compact_layout(const moe_shape *s, size_t *mid, size_t *y) {
+    const size_t T = (size_t)std::max(s->T, 0), K = (size_t)std::max(s->K, 0), Ucap = T * (K + 1);
+    const size_t Imax = (size_t)std::max(s->I, s->I_shared), H = (size_t)s->H;
+    *mid = sizeof(moe::WsHeader);
+    *y = align_up(*mid + Ucap * Imax * sizeof(float), 256);
+    return align_up(*y + Ucap * H * sizeof(float), 256);
+}
+
+// fma_compact: the caller's buffer serves the CUDA-core kernel alone (the
+// no-allocation entry), with its scratch laid out by fma_compact_layout.
 moe_status fused_decode_impl(const void *x, const int32_t *ids, const float *w,
                              const moe_weights *routed, const moe_weights *shared, void *out,
-                             const moe_shape *s, void *ws, size_t ws_bytes, cudaStream_t stream) {
+                             const moe_shape *s, void *ws, size_t ws_bytes, cudaStream_t stream,
+                             bool fma_compact = false) {
     moe_status st = check_shape(s);
     if (st != MOE_OK) return st;
     if ((st = check_weights(routed, "routed")) != MOE_OK) return st;
     if ((st = check_weights(shared, "shared")) != MOE_OK) return st;
     if (!ws) return fail(MOE_ERR_INVALID_ARG, "workspace is NULL");
     if (!aligned(ws, 256)) return fail(MOE_ERR_INVALID_ARG, "workspace not 256-byte aligned");
+    // host-only checks first: nothing below them touches the device until
+    // the arguments are known to be valid
     const WsLayout L = ws_layout(s);
-    const char *why = "";
-    const bool tc_ok = tc_eligible(s, routed, shared, &why);
-    bool use_tc = tc_ok && !(s->flags & MOE_FLAG_FORCE_FMA);
-    if ((s->flags & MOE_FLAG_FORCE_MMA) && !tc_ok)
-        return fail(MOE_ERR_UNSUPPORTED, "tensor-core path requested but unavailable: %s", why);
-    const size_t need = use_tc ? L.tc_end : L.fma_end;
-    if (ws_bytes < need)
-        return fail(MOE_ERR_WORKSPACE, "workspace has %zu B, needs %zu B", ws_bytes, need);
+    size_t mid_off = L.mid, y_off = L.y, fma_need = L.fma_end;
+    if (fma_compact) fma_need = fma_compact_layout(s, &mid_off, &y_off);
+    const bool force_fma = fma_compact || (s->flags & MOE_FLAG_FORCE_FMA);
+    const size_t need_min = force_fma ? fma_need : std::min(fma_need, L.tc_end);
+    if (ws_bytes < need_min)
+        return fail(MOE_ERR_WORKSPACE, "workspace has %zu B, needs %zu B", ws_bytes, need_min);
     if (s->T == 0) return MOE_OK;
     if (!x || !out || !ids || !w) return fail(MOE_ERR_INVALID_ARG, "NULL x/out/topk_ids/topk_w");
     if (!aligned(x, 16) || !aligned(out, 16))
@@ -483,6 +532,19 @@ moe_status fused_decode_impl(const void *x, const int32_t *ids, const float *w,
     const uintptr_t xa = (uintptr_t)x, oa = (uintptr_t)out;
     if (xa < oa + act_bytes && oa < xa + act_bytes)
         return fail(MOE_ERR_INVALID_ARG, "out overlaps x");
+    // the path: tensor cores where eligible (a device fact: shared memory)
+    int dev = 0;
+    if ((st = current_device(&dev)) != MOE_OK) return st;
+    DevInfo d;
+    if ((st = dev_info(dev, &d)) != MOE_OK) return st;
+    const char *why = "this entry runs the CUDA-core contraction";
+    const bool tc_ok = !fma_compact && tc_eligible(s, routed, shared, d, &why);
+    bool use_tc = tc_ok && !(s->flags & MOE_FLAG_FORCE_FMA);
+    if ((s->flags & MOE_FLAG_FORCE_MMA) && !tc_ok)
+        return fail(MOE_ERR_UNSUPPORTED, "tensor-core path requested but unavailable: %s", why);
+    const size_t need = use_tc ? L.tc_end : fma_need;
+    if (ws_bytes < need)
+        return fail(MOE_ERR_WORKSPACE, "workspace has %zu B, needs %zu B", ws_bytes, need);
 
     moe::FusedParams p;
     p.x = static_cast<const __nv_bfloat16 *>(x);
@@ -499,11 +561,11 @@ moe_status fused_decode_impl(const void *x, const int32_t *ids, const float *w,
     p.K = s->K;
     p.flags = s->flags;
     p.hdr = static_cast<moe::WsHeader *>(ws);
-    p.mid = reinterpret_cast<float *>(static_cast<char *>(ws) + L.mid);
-    p.y = reinterpret_cast<float *>(static_cast<char *>(ws) + L.y);
+    p.mid = reinterpret_cast<float *>(static_cast<char *>(ws) + mid_off);
+    p.y = reinterpret_cast<float *>(static_cast<char *>(ws) + y_off);
     p.Imax = std::max(s->I, s->I_shared);
-    if (use_tc) return launch_fused_tc(p, L, s, routed, shared, stream);
-    return launch_fused_fma(p, s, stream);
+    if (use_tc) return launch_fused_tc(p, L, s, routed, shared, dev, d, stream);
+    return launch_fused_fma(p, s, dev, d, stream);
 }
 
 }  // namespace
@@ -519,27 +581,70 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 
 namespace {
 
-constexpr int kNoAllocMaxDevices = 64;
-std::mutex g_noalloc_mu;
-void *g_noalloc_addr[kNoAllocMaxDevices] = {};
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
 
-// Device address of g_noalloc_scratch on the current device; looked up once
-// per device, with that device current, on its first call.
-moe_status noalloc_scratch(void **out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    if (dev < 0 || dev >= kNoAllocMaxDevices)
-        return fail(MOE_ERR_UNSUPPORTED, "device %d: the no-allocation entry handles devices 0..%d",
-                    dev, kNoAllocMaxDevices - 1);
-    std::lock_guard<std::mutex> lk(g_noalloc_mu);
-    if (!g_noalloc_addr[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(no-allocation scratch)");
-        g_noalloc_addr[dev] = p;
+// Unique id of the CUDA context current on this thread (ids are never reused
+// within a process, unlike context handles after a device reset).
+moe_status current_context_id(unsigned long long *id) {
+    static CtxGetCurrentFn get_cur = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::mutex mu;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        if (!get_cur || !get_id) {
+            cudaDriverEntryPointQueryResult q;
+            void *p1 = nullptr, *p2 = nullptr;
+            cudaError_t e = cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p1, 12000, cudaEnableDefault, &q);
+            if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !p1)
+                return fail(MOE_ERR_CUDA, "cuCtxGetCurrent is not available from the driver");
+            e = cudaGetDriverEntryPointByVersion("cuCtxGetId", &p2, 12000, cudaEnableDefault, &q);
+            if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !p2)
+                return fail(MOE_ERR_CUDA, "cuCtxGetId is not available from the driver");
+            get_cur = (CtxGetCurrentFn)p1;
+            get_id = (CtxGetIdFn)p2;
+        }
     }
-    *out = g_noalloc_addr[dev];
+    CUcontext ctx = nullptr;
+    if (get_cur(&ctx) != CUDA_SUCCESS || !ctx) return fail(MOE_ERR_CUDA, "no current CUDA context");
+    if (get_id(ctx, id) != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuCtxGetId failed");
+    return MOE_OK;
+}
+
+// Device address of g_noalloc_scratch in the current context: looked up with
+// cudaGetSymbolAddress the first time a context calls (its device current),
+// then cached under the context's unique id, so a context created later (for
+// example after a device reset) gets its own lookup.
+moe_status noalloc_scratch(void **out) {
+    struct Entry {
+        unsigned long long ctx;
+        void *addr;
+    };
+    constexpr int kEntries = 64;
+    static Entry cache[kEntries];
+    static int used = 0, next = 0;
+    static std::mutex mu;
+    unsigned long long ctx = 0;
+    bool have_ctx = current_context_id(&ctx) == MOE_OK;
+    std::lock_guard<std::mutex> lk(mu);
+    if (have_ctx)
+        for (int i = 0; i < used; ++i)
+            if (cache[i].ctx == ctx) {
+                *out = cache[i].addr;
+                return MOE_OK;
+            }
+    // first call in this context (the lookup also makes the runtime's context
+    // current when no context was)
+    void *p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(no-allocation scratch)");
+    if (!have_ctx) {
+        moe_status st = current_context_id(&ctx);
+        if (st != MOE_OK) return st;
+    }
+    const int slot = used < kEntries ? used++ : (next++ % kEntries);
+    cache[slot] = {ctx, p};
+    *out = p;
     return MOE_OK;
 }
 
@@ -580,8 +685,10 @@ moe_status moe_group_table(const int32_t *topk_ids, const moe_shape *s, int32_t 
     if (workspace_bytes < sizeof(moe::WsHeader))
         return fail(MOE_ERR_WORKSPACE, "workspace smaller than its header");
     if (s->T > 0 && !topk_ids) return fail(MOE_ERR_INVALID_ARG, "topk_ids is NULL");
+    int dev = 0;
+    if ((st = current_device(&dev)) != MOE_OK) return st;
     DevInfo d;
-    if ((st = dev_info(&d)) != MOE_OK) return st;
+    if ((st = dev_info(dev, &d)) != MOE_OK) return st;
     const size_t smem = table_smem_bytes(s);
     if ((st = set_smem(moe::group_table_kernel, smem, d)) != MOE_OK) return st;
     moe::group_table_kernel<<<1, 256, smem, (cudaStream_t)stream>>>(
@@ -640,11 +747,12 @@ moe_status moe_fused_decode_noalloc(const void *x, const int32_t *topk_ids, cons
                                     void *stream) {
     moe_status st = check_shape(s);
     if (st != MOE_OK) return st;
-    // the built-in scratch serves the CUDA-core contraction, whose scratch is
-    // the smaller one (the fp32 intermediates only)
+    // the built-in scratch serves the CUDA-core contraction alone, laid out
+    // straight after the header (its fp32 intermediates are the smaller scratch)
     moe_shape sf = *s;
     sf.flags = (sf.flags & ~(unsigned)MOE_FLAG_FORCE_MMA) | MOE_FLAG_FORCE_FMA;
-    const size_t need = ws_layout(&sf).fma_end;
+    size_t mid_off = 0, y_off = 0;
+    const size_t need = fma_compact_layout(&sf, &mid_off, &y_off);
     if (need > kNoAllocScratchBytes)
         return fail(MOE_ERR_WORKSPACE,
                     "this shape needs %zu B of scratch; the no-allocation entry's built-in "
@@ -657,7 +765,7 @@ moe_status moe_fused_decode_noalloc(const void *x, const int32_t *topk_ids, cons
     // The header must be zero when the kernel starts. The array is zero when
     // the library loads, and every call below leaves it zero again.
     st = fused_decode_impl(x, topk_ids, topk_w, routed, shared, out, &sf, scratch,
-                           kNoAllocScratchBytes, cs);
+                           kNoAllocScratchBytes, cs, true);
     if (st != MOE_OK) return st;
     cudaError_t e;
     if (err_out &&

@@ -12,7 +12,7 @@ import oracle
 from moe_layer_decode_persistent_b300 import binding as B
 from moe_layer_decode_persistent_b300 import inputs
 
-from gpu_util import ensure_built, layer, run_fused, shape_of
+from gpu_util import assert_parity, ensure_built, layer, oracle_ref, run_fused, shape_of
 
 pytestmark = pytest.mark.gpu
 
@@ -33,6 +33,26 @@ def test_noalloc_matches_workspace_entry_on_two_calls_in_a_row():
         assert ok, f"no-alloc output differs beyond tolerance (ratio {ratio:.3f})"
         assert torch.equal(out.view(torch.int16), want_fma.view(torch.int16))
         assert int(err.item()) == 0
+    assert_parity(out, oracle_ref(L))
+
+
+def test_noalloc_size_limit_is_exact_at_dsv3_shapes():
+    """The built-in 8 MiB scratch holds DeepSeek-V3 shapes up to T=25: T=25
+    runs (and matches the workspace entry's CUDA-core result bit for bit),
+    T=26 is refused with MOE_ERR_WORKSPACE before anything is launched."""
+    ensure_built()
+    L = layer(inputs.dsv3(25), "uniform", seed=13)
+    want = run_fused(L, B.MOE_FLAG_FORCE_FMA)
+    rw, sw = B.make_weights(L.routed), B.make_weights(L.shared)
+    out = torch.full_like(want, float("nan"))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.moe_fused_decode_noalloc(L.x, L.topk_ids, L.topk_w, rw, sw, out, shape_of(L), err_out=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(out.view(torch.int16), want.view(torch.int16))
+    big = B.make_shape(26, 7168, 2048, 2048, 256, 8, 0)
+    st = B.moe_fused_decode_noalloc(L.x, L.topk_ids, L.topk_w, rw, sw, out, big, check=False)
+    assert st == B.MOE_ERR_WORKSPACE
 
 
 def test_noalloc_reports_device_error_bits_and_rejects_large_shapes():
