@@ -681,6 +681,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
             }
             if (!ok) break;
         }
+        cp_async_wait_all();  // no copy into shared memory outlives the role
     } else if (warp < 2 + kIssuers) {
         // ===================== MMA issuers (warps 2-5) =====================
         if (lane == 0) {
@@ -861,6 +862,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
             }
             if (!ok) break;
         }
+        tmem_wait_st();  // an aborted stage may leave TMEM stores in flight
     } else {
         // ===================== epilogue (the last 4 warps) =====================
         // Each warp owns 32 rows of the tile (its TMEM lane quarter) and runs
@@ -870,6 +872,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
         const int r = (quarter << 5) | lane;
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
         int js = 0, jph = 0, ds = 0, dph = 0;
+        // fault injection (MOE_FLAG_DEBUG_DROP_ARRIVE): CTA 0's first quarter
+        // skips its first intermediate-ready arrival, so the down jobs of that
+        // (group, column tile) wait out their budget and the launch aborts
+        bool drop_next = (p.flags & kFlagDebugDropArrive) && blockIdx.x == 0 && quarter == 0;
         for (;;) {
             if (!__all_sync(0xffffffffu, mbar_wait(&jfull[js], jph, abort_flag, err))) break;
             const TcJob d = job_at(js);
@@ -1030,7 +1036,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                 if (have_mid) {
                     __threadfence();
                     __syncwarp();
-                    if (lane == 0) atom_add_acq_rel_gpu(group_ready + d.pair, 1u);
+                    if (lane == 0 && !drop_next) atom_add_acq_rel_gpu(group_ready + d.pair, 1u);
+                    drop_next = false;
                 }
             } else {
                 // ---- down phase 2: count this (job, quarter) on its 256-row tile;

@@ -144,6 +144,9 @@ __device__ __forceinline__ void cp_async16(void *dst, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
 
+// Wait until all of this thread's cp.async copies have landed.
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // The mbarrier receives one arrival (counted against its expected count)
 // once all of this thread's earlier cp.async copies have landed.
 __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {
