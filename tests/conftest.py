@@ -25,3 +25,22 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Worst |gpu - ref| / bound of each GPU parity check against the oracle
+    (bound = 2^-7 |ref| + 1e-3 rms(ref)); 1.0 is the tolerance's edge."""
+    mod = sys.modules.get("gpu_util")
+    ratios = getattr(mod, "RATIOS", None) if mod else None
+    if not ratios:
+        return
+    worst = {}
+    for test, r, n in ratios:
+        w, m = worst.get(test, (0.0, 0))
+        worst[test] = (max(w, r), m + n)
+    tr = terminalreporter
+    tr.write_sep("-", "parity against the oracle: worst |err|/bound per test")
+    for test, (r, n) in sorted(worst.items(), key=lambda kv: -kv[1][0]):
+        tr.write_line(f"{r:6.3f}  {n:>9d} elements  {test}")
+    tr.write_line(f"overall worst {max(r for r, _ in worst.values()):.3f} over "
+                  f"{sum(n for _, n in worst.values())} elements in {len(worst)} tests")

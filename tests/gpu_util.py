@@ -78,11 +78,18 @@ def oracle_ref(L, rows=None, threads=None):
                             s.I_shared, max(len(used), 1), s.K, rows=rows, threads=threads)
 
 
+# (test id, worst |err|/bound, elements compared) of every parity check in
+# this session; conftest prints them at the end of the run
+RATIOS = []
+
+
 def assert_parity(out, ref, rows=None):
     got = out.float().cpu().double().numpy()
     if rows is not None:
         got = got[np.asarray(rows)]
     ok, ratio = oracle.tolerance_ok(got, ref)
+    test = os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0]
+    RATIOS.append((test, ratio, int(np.asarray(ref).size)))
     assert ok, f"tolerance exceeded: worst |err|/bound = {ratio:.3f}"
     return ratio
 

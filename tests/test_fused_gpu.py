@@ -59,12 +59,18 @@ def test_dsv3_t8_mtp_full(path):
     assert_parity(run_fused(L, PATHS[path]), oracle_ref(L))
 
 
-@pytest.mark.parametrize("path", list(PATHS))
-def test_dsv3_t64_zipf_sampled_rows(path):
+@pytest.fixture(scope="module")
+def dsv3_t64():
+    """DSv3 T=64 Zipf layer and its fp64 oracle output on every row."""
     L = layer(inputs.dsv3(64), "zipf", seed=0)
-    rows = [0, 17, 38, 63]
+    return L, oracle_ref(L)
+
+
+@pytest.mark.parametrize("path", list(PATHS))
+def test_dsv3_t64_zipf_all_rows(path, dsv3_t64):
+    L, ref = dsv3_t64
     out = run_fused(L, PATHS[path])
-    assert_parity(out, oracle_ref(L, rows=rows), rows=rows)
+    assert_parity(out, ref)
     assert torch.isfinite(out.float()).all()
 
 
@@ -87,12 +93,18 @@ def wide_t256():
     return layer(inputs.dsv3(256, E=384), "uniform", seed=0)
 
 
+WIDE_ROWS = [int(r) for r in np.linspace(0, 255, 32).round()]
+
+
+@pytest.fixture(scope="module")
+def wide_t256_ref(wide_t256):
+    return oracle_ref(wide_t256, rows=WIDE_ROWS)
+
+
 @pytest.mark.parametrize("path", ["mma", "auto"])
-def test_wide_expert_T256_sampled_rows(path, wide_t256):
-    L = wide_t256
-    rows = [0, 101, 255]
-    out = run_fused(L, PATHS[path])
-    assert_parity(out, oracle_ref(L, rows=rows), rows=rows)
+def test_wide_expert_T256_32_spread_rows(path, wide_t256, wide_t256_ref):
+    out = run_fused(wide_t256, PATHS[path])
+    assert_parity(out, wide_t256_ref, rows=WIDE_ROWS)
     assert torch.isfinite(out.float()).all()
 
 
@@ -140,6 +152,27 @@ def test_paths_and_shapes_take_turns_on_one_workspace():
              ("t1", "mma"), ("t1", "mma"), ("t8", "fma"), ("t8", "mma")]
     for n, p in order:
         out = run_fused(L8 if n == "t8" else L1, PATHS[p], ws=ws)
+        assert torch.equal(out.view(torch.int16), ref[(n, p)].view(torch.int16)), (n, p)
+
+
+def test_k_and_intermediate_changes_take_turns_on_one_workspace():
+    """Launches of different K, I and I_shared (and both paths) on one
+    workspace sized for the largest of them give the results of fresh
+    workspaces, bit for bit: the tensor path's counters sit at fixed offsets
+    that no shape's scratch covers."""
+    shapes = {"k8": inputs.Shape(T=16, H=512, I=256, I_shared=512, E=16, K=8),
+              "k4": inputs.Shape(T=16, H=512, I=256, I_shared=512, E=16, K=4),
+              "i512": inputs.Shape(T=8, H=512, I=512, I_shared=256, E=16, K=8),
+              "t3": inputs.Shape(T=3, H=512, I=256, I_shared=256, E=16, K=5)}
+    Ls = {n: layer(s, "zipf", seed=i + 20, used_only=False) for i, (n, s) in enumerate(shapes.items())}
+    nbytes = max(B.moe_workspace_bytes(shape_of(L)) for L in Ls.values())
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    B.moe_workspace_init(ws)
+    ref = {(n, p): run_fused(L, PATHS[p]) for n, L in Ls.items() for p in ("mma", "fma")}
+    order = [("k8", "mma"), ("k4", "mma"), ("k8", "mma"), ("i512", "mma"), ("k8", "fma"), ("k8", "mma"),
+             ("t3", "mma"), ("k4", "fma"), ("i512", "mma"), ("k8", "mma"), ("t3", "fma"), ("k4", "mma")]
+    for n, p in order:
+        out = run_fused(Ls[n], PATHS[p], ws=ws)
         assert torch.equal(out.view(torch.int16), ref[(n, p)].view(torch.int16)), (n, p)
 
 
@@ -198,35 +231,60 @@ def test_zero_down_weights_give_residual(path):
     assert torch.equal(out.view(torch.int16), L.x.view(torch.int16))
 
 
-def test_bad_and_repeated_ids_set_error_bits():
-    s = inputs.Shape(T=4, H=256, I=128, I_shared=128, E=8, K=2)
-    L = layer(s, "uniform", seed=7, used_only=False)
+# H, I and I_shared multiples of 256: the tensor-core path is eligible
+ELIGIBLE = inputs.Shape(T=4, H=512, I=256, I_shared=256, E=8, K=2)
+
+
+@pytest.mark.parametrize("path", list(PATHS))
+def test_bad_and_repeated_ids_set_error_bits(path):
+    """An id outside [0, E) sets MOE_DEV_BAD_EXPERT and adds nothing; an id
+    repeated within a row sets MOE_DEV_DUP_EXPERT and both uses count. Each is
+    checked against the oracle, and the dedup form stays bitwise equal to the
+    one-row form."""
+    L = layer(ELIGIBLE, "uniform", seed=7, used_only=False)
     ref_ok = oracle_ref(L)
     L.topk_ids[1, 1] = 99
+    L.topk_ids[2, 0] = -1
     ws = workspace(L)
-    out = run_fused(L, 0, ws=ws, check_err=False)
+    out = run_fused(L, PATHS[path], ws=ws, check_err=False)
     assert B.moe_read_error(ws) == B.MOE_DEV_BAD_EXPERT
     ref = oracle_ref(L)
     assert_parity(out, ref)
-    assert not np.array_equal(ref[1], ref_ok[1])
+    assert not np.array_equal(ref[1], ref_ok[1]) and not np.array_equal(ref[2], ref_ok[2])
+    one_row = run_fused(L, PATHS[path] | B.MOE_FLAG_NO_DEDUP, ws=ws, check_err=False)
+    assert B.moe_read_error(ws) == B.MOE_DEV_BAD_EXPERT
+    assert torch.equal(out.view(torch.int16), one_row.view(torch.int16))
     L.topk_ids[1, 1] = L.topk_ids[1, 0]
-    out = run_fused(L, 0, ws=ws, check_err=False)
+    L.topk_ids[2, 0] = L.topk_ids[2, 1]
+    out = run_fused(L, PATHS[path], ws=ws, check_err=False)
     assert B.moe_read_error(ws) == B.MOE_DEV_DUP_EXPERT
     assert_parity(out, oracle_ref(L))
+    one_row = run_fused(L, PATHS[path] | B.MOE_FLAG_NO_DEDUP, ws=ws, check_err=False)
+    assert B.moe_read_error(ws) == B.MOE_DEV_DUP_EXPERT
+    assert torch.equal(out.view(torch.int16), one_row.view(torch.int16))
 
 
-def test_dropped_arrival_times_out_and_workspace_recovers():
+@pytest.mark.parametrize("path", ["fma", "mma"])
+def test_dropped_arrival_times_out_and_workspace_recovers(path):
     """Fault injection on the host side of the protocol: one CTA skips an
-    arrival, every wait runs out after its budget and sets the timeout bit;
-    the context stays usable and a re-initialised workspace works again."""
-    s = inputs.Shape(T=2, H=256, I=128, I_shared=128, E=8, K=2)
+    arrival (CUDA-core kernel: a grid barrier arrival; tensor-core kernel: an
+    intermediate-ready arrival), the waits on it run out after their budget and
+    set the timeout bit, every role stops and frees what it holds; the context
+    stays usable and a re-initialised workspace gives the same output as a
+    fresh one."""
+    s = ELIGIBLE if path == "mma" else inputs.Shape(T=2, H=256, I=128, I_shared=128, E=8, K=2)
     L = layer(s, "uniform", seed=8, used_only=False)
     ws = workspace(L)
-    run_fused(L, B.MOE_FLAG_DEBUG_DROP_ARRIVE, ws=ws, check_err=False)
+    run_fused(L, PATHS[path] | B.MOE_FLAG_DEBUG_DROP_ARRIVE, ws=ws, check_err=False)
     assert B.moe_read_error(ws) & B.MOE_DEV_WAIT_TIMEOUT
     B.moe_workspace_init(ws)
-    out = run_fused(L, 0, ws=ws)
+    out = run_fused(L, PATHS[path], ws=ws)
     assert_parity(out, oracle_ref(L))
+    fresh = run_fused(L, PATHS[path])
+    assert torch.equal(out.view(torch.int16), fresh.view(torch.int16))
+    # and the workspace serves later launches too
+    again = run_fused(L, PATHS[path], ws=ws)
+    assert torch.equal(again.view(torch.int16), fresh.view(torch.int16))
 
 
 def test_host_buffer_entry_matches_device_entry():
