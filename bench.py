@@ -2,7 +2,7 @@
 HBM GB/s against the byte roofline, one JSON line on stdout.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload dsv3_t1|dsv3_t8|dsv3_t64] [--sweep] [--sweep-wide]
+                  [--workload dsv3_t1|dsv3_t8|dsv3_t64] [--no-sweep] [--sweep-wide]
 
 A step is one launch of the whole layer (group table, gate/up + SwiGLU,
 down, router weights, shared expert, residual, bf16 write) over one batch.
@@ -11,10 +11,10 @@ routed I=2048 NVFP4 E=256 top-8, shared I=2048 FP8 128x128 blocks, uniform
 routing). Four copies of the layer's weights are resident and the steps
 rotate over them, so each step reads weights that are not in L2 (126 MB).
 Every timing is also taken with the launches captured in a CUDA graph and
-replayed (`graph_us_per_launch`). --sweep adds the T=8 and T=64 workloads;
---sweep-wide the wide-expert layer (E=384 top-8, uniform routing) at
+replayed (`graph_us_per_launch`). The T=8 and T=64 workloads are timed too, under `sweep`
+(--no-sweep skips them); --sweep-wide adds the wide-expert layer (E=384 top-8, uniform routing) at
 T = 1, 2, 4, ..., 256 with 4 distinct layers' weights resident, run back to
-back. --impl reference times the fp64 CPU oracle on a bounded sample of the
+back. --impl reference times the fp64 CPU oracle on whole launches of the
 same workload (the reference arm). Under torchrun every rank runs its own replica
 (the build has no cross-GPU exchange); rank 0 prints the max over ranks.
 """
@@ -224,6 +224,10 @@ def run_ours(args, rank, world, local):
         rw, sw = weights[i % len(weights)]
         B.moe_fused_decode(L.x, L.topk_ids, L.topk_w, rw, sw, out, sh, ws, stream=stream)
 
+    # the clock sampler starts before the warm-up (its start-up pause would
+    # otherwise leave the GPU idle right before the timed region) and runs
+    # until the last GPU timing of this bench
+    clk = ClockSampler(local).__enter__()
     for i in range(args.warmup):
         launch(i)
     torch.cuda.synchronize()
@@ -233,16 +237,15 @@ def run_ours(args, rank, world, local):
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        t0 = torch.cuda.Event(enable_timing=True)
-        t1 = torch.cuda.Event(enable_timing=True)
-        t0.record(stream)
-        for i in range(args.steps):
-            starts[i].record(stream)
-            launch(i)
-            ends[i].record(stream)
-        t1.record(stream)
-        torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        starts[i].record(stream)
+        launch(i)
+        ends[i].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
     barrier(world)
     err = B.moe_read_error(ws)
     per_launch = [s.elapsed_time(e) * 1e3 for s, e in zip(starts, ends)]  # us
@@ -253,9 +256,10 @@ def run_ours(args, rank, world, local):
 
     # end to end through the host-buffer entry point (pinned buffers, copies inside)
     if args.no_e2e:
+        clk.__exit__()
         return dict(us_launch=us_launch_max, ms_per_step=ms_per_step, algo_bytes=algo_bytes,
                     distinct=distinct, clocks=clk.summary(), err=err, e2e_us=None, h2d=0, d2h=0,
-                    sweep={}, wide={}, graph_us=None, T=shape.T)
+                    sweep={}, wide={}, graph_us=None, T=shape.T, per_launch=per_launch)
     xh = L.x.cpu().pin_memory()
     ih = L.topk_ids.cpu().pin_memory()
     wh = L.topk_w.cpu().pin_memory()
@@ -282,17 +286,21 @@ def run_ours(args, rank, world, local):
     graph_us = graph_us_per_launch(launch_s, 4 * len(weights))
     assert B.moe_read_error(ws) == 0
 
+    # the other workloads of the metric (T=8, T=64), unless --no-sweep
+    del copies, weights
+    torch.cuda.empty_cache()
     sweep = {}
-    if args.sweep:
+    if not args.no_sweep:
         for name in WORKLOADS:
             if name == args.workload:
                 continue
             sweep[name] = sweep_point(name, args, dev)
     wide = wide_sweep(args, dev) if args.sweep_wide else {}
+    clk.__exit__()
     return dict(us_launch=us_launch_max, ms_per_step=ms_per_step, algo_bytes=algo_bytes,
                 distinct=distinct, clocks=clk.summary(), err=err, e2e_us=e2e_us,
                 h2d=xh.numel() * 2 + ih.numel() * 4 + wh.numel() * 4, d2h=oh.numel() * 2,
-                sweep=sweep, wide=wide, graph_us=graph_us, T=shape.T)
+                sweep=sweep, wide=wide, graph_us=graph_us, T=shape.T, per_launch=per_launch)
 
 
 def graph_us_per_launch(launch, n_launch: int, reps: int = 5) -> float:
@@ -329,8 +337,9 @@ def sweep_point(name, args, dev):
     from moe_layer_decode_persistent_b300 import binding as B
     from moe_layer_decode_persistent_b300 import inputs
     wl = WORKLOADS[name]
-    shape = inputs.dsv3(wl["T"])
-    L = inputs.make_layer(shape, wl["routing"], 0, dev, inputs.FMT_NVFP4, inputs.FMT_FP8_B128)
+    shape = inputs.dsv3(wl["T"], E=args.experts)
+    L = inputs.make_layer(shape, wl["routing"], 0, dev, inputs.FMT_NVFP4, inputs.FMT_FP8_B128,
+                          used_only=True)
     copies = [(L.routed, L.shared)] + [
         (inputs.ExpertSet(**{k: (v.clone() if isinstance(v, torch.Tensor) else v)
                              for k, v in L.routed.__dict__.items()}), L.shared)
@@ -342,7 +351,7 @@ def sweep_point(name, args, dev):
     out = torch.empty(shape.T, shape.H, dtype=torch.bfloat16, device=dev)
     for i in range(3):
         B.moe_fused_decode(L.x, L.topk_ids, L.topk_w, *weights[i % N_COPIES], out, sh, ws)
-    n = max(10, args.steps // 2)
+    n = max(20, args.steps // 2)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
     torch.cuda.synchronize()
     for i in range(n):
@@ -364,7 +373,9 @@ def sweep_point(name, args, dev):
     del L, copies, weights
     torch.cuda.empty_cache()
     return {"us_per_launch": round(us, 2), "graph_us_per_launch": round(g_us, 2), "hbm_gbs": round(gbs, 1),
-            "frac": round(gbs / peak, 4), "distinct_experts": distinct, "algo_bytes": b}
+            "frac": round(gbs / peak, 4), "frac_graph": round(b / (g_us * 1e-6) / 1e9 / peak, 4),
+            "distinct_experts": distinct, "algo_bytes": b, "launches": n, "T": wl["T"],
+            "routing": wl["routing"]}
 
 
 WIDE_T = [1, 2, 4, 8, 16, 32, 64, 128, 256]
@@ -428,57 +439,84 @@ def wide_sweep(args, dev, n_layers: int = 4):
     return res
 
 
-def oracle_sample(workload: str, n_experts_per_step: int = 1):
-    """A bounded sample of the workload for the CPU oracle: the first rows'
-    expert uses (expert FFNs), and the scale factor to a whole layer launch."""
+def oracle_launch(workload: str):
+    """One whole launch of the workload for the CPU oracle: the batch's inputs
+    and the experts it uses (drawn on the host with the GPU arm's recipe, the
+    routed ones stored compactly), and a callable that runs the oracle on every
+    row with the given thread count. Returns (run, expert uses per launch)."""
     import numpy as np
 
     import oracle
     from moe_layer_decode_persistent_b300 import inputs
     wl = WORKLOADS[workload]
     shape = inputs.dsv3(wl["T"])
-    ids = inputs.ROUTINGS[wl["routing"]](shape.T, shape.K, shape.E, 0).numpy()
-    e = int(ids[0, 0])
-    routed = inputs.make_experts(inputs.FMT_NVFP4, 1, shape.H, shape.I, ("L", 0, 0), "cpu",
-                                 tag="routed")  # one expert's bytes stand in for expert e
-    ws = oracle.WeightSet(routed.fmt, routed.w13, routed.w2, routed.w13_scale, routed.w2_scale,
-                          routed.w13_gscale, routed.w2_gscale)
-    x = inputs.activations(1, shape.H, 0).double().numpy()[0]
-    uses = shape.T * shape.K + shape.T  # expert FFN evaluations in one layer launch
-    return (lambda: oracle.expert_ffn(ws, shape.H, shape.I, 0, x)), uses, e
+    ids = inputs.ROUTINGS[wl["routing"]](shape.T, shape.K, shape.E, 0)
+    used = sorted(set(int(e) for e in ids.reshape(-1).tolist()))
+    remap = {e: i for i, e in enumerate(used)}
+    ids_c = ids.clone()
+    for t in range(shape.T):
+        for p in range(shape.K):
+            ids_c[t, p] = remap[int(ids[t, p])]
+    routed = inputs.make_expert_subset(inputs.FMT_NVFP4, used, shape.H, shape.I, ("L", 0, 0), "cpu")
+    shared = inputs.make_experts(inputs.FMT_FP8_B128, 1, shape.H, shape.I_shared, ("L", 0, 0), "cpu",
+                                 tag="shared")
+
+    def wset(es):
+        return oracle.WeightSet(es.fmt, es.w13, es.w2, es.w13_scale, es.w2_scale, es.w13_gscale, es.w2_gscale)
+
+    rw, sw = wset(routed), wset(shared)
+    x = inputs.activations(shape.T, shape.H, 0)
+    w = inputs.router_weights(shape.T, shape.K, 0)
+    uses = shape.T * (shape.K + 1)
+
+    def run(threads):
+        out = oracle.moe_layer_uses(x, ids_c, w, rw, sw, shape.T, shape.H, shape.I, shape.I_shared,
+                                    len(used), shape.K, threads=threads)
+        assert np.isfinite(out).all()
+
+    return run, uses
 
 
-def run_reference(args, rank, world):
+def oracle_threads(uses: int) -> int:
+    return max(1, min(uses, os.cpu_count() or 1))
+
+
+def run_reference(args):
+    """The reference arm: the fp64 oracle, one whole launch of the workload
+    per step, its expert evaluations spread over the host's cores."""
     import oracle
     oracle.build()
-    fn, uses, _ = oracle_sample(args.workload)
-    for _ in range(max(1, min(args.warmup, 1))):
-        fn()
+    run, uses = oracle_launch(args.workload)
+    threads = oracle_threads(uses)
+    for _ in range(args.warmup):
+        run(threads)
     times = []
     for _ in range(args.steps):
         t = time.perf_counter()
-        fn()
+        run(threads)
         times.append(time.perf_counter() - t)
-    per_ffn = statistics.mean(times)
-    us_layer = per_ffn * uses * 1e6
-    return us_layer, per_ffn, uses
+    return statistics.mean(times) * 1e6, threads, uses
 
 
 def cpu_baseline(args):
-    """The oracle as it stands, timed on this host on a bounded sample."""
+    """The oracle as it stands, timed on this host: whole launches of the
+    workload (all rows, every expert use), repeated for about 10 s."""
     import oracle
     oracle.build()
-    fn, uses, _ = oracle_sample(args.workload)
+    run, uses = oracle_launch(args.workload)
+    threads = oracle_threads(uses)
+    run(threads)  # first touch of the weights
     t = time.perf_counter()
     n = 0
-    while n < 3 or time.perf_counter() - t < 8.0:
-        fn()
+    while n < 1 or time.perf_counter() - t < 10.0:
+        run(threads)
         n += 1
-    per_ffn = (time.perf_counter() - t) / n
-    return {"value": round(per_ffn * uses * 1e6, 1), "unit": "us", "cores": 1, "kind": "oracle",
-            "sample": f"{n} single-row expert FFNs (dequant + SwiGLU + down, fp64) of one NVFP4 "
-                      f"DSv3 expert, scaled by the {uses} expert uses of one {args.workload} "
-                      f"launch; the oracle is single-threaded per row"}
+    us = (time.perf_counter() - t) / n * 1e6
+    return {"value": round(us, 1), "unit": "us", "cores": threads, "host_cpus": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"{n} whole {args.workload} launches (every row, {uses} expert evaluations "
+                      f"each: dequant + SwiGLU + down in fp64, then the fixed-order sum), the "
+                      f"evaluations of a launch spread over {threads} threads"}
 
 
 def main():
@@ -489,7 +527,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=list(WORKLOADS), default="dsv3_t1")
     ap.add_argument("--flags", type=int, default=0)
-    ap.add_argument("--sweep", action="store_true", help="also time the T=8 and T=64 workloads")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the T=8 and T=64 workloads (timed by default, under `sweep`)")
     ap.add_argument("--sweep-wide", action="store_true",
                     help="also time the wide-expert layer (E=384) at T=1..256, 4 layers back to back")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -510,17 +549,18 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        us_layer, per_ffn, uses = run_reference(args, rank, world)
-        line = {"impl": "reference", "metric": metric, "value": round(us_layer, 1), "unit": "us",
+        us_launch, threads, uses = run_reference(args)
+        line = {"impl": "reference", "metric": metric, "value": round(us_launch, 1), "unit": "us",
                 "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-                "ms_per_step": round(us_layer / 1e3, 3), "higher_is_better": False,
-                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": config,
-                "cpu_baseline": {"value": round(us_layer, 1), "unit": "us", "cores": 1,
-                                 "kind": "oracle",
-                                 "sample": f"per step one single-row NVFP4 expert FFN in fp64, "
-                                           f"scaled by the {uses} expert uses of a launch"},
-                "e2e": {"value": round(us_layer, 1), "unit": "us", "h2d_bytes_per_step": 0,
+                "ms_per_step": round(us_launch / 1e3, 3), "higher_is_better": False,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic (the same recipe, drawn on the host)", "config": config,
+                "cpu_baseline": {"value": round(us_launch, 1), "unit": "us", "cores": threads,
+                                 "host_cpus": os.cpu_count(), "kind": "oracle",
+                                 "sample": f"every step one whole {args.workload} launch of the fp64 "
+                                           f"oracle ({uses} expert evaluations over {threads} "
+                                           f"threads, then the fixed-order sum of every row)"},
+                "e2e": {"value": round(us_launch, 1), "unit": "us", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
         return

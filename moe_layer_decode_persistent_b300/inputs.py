@@ -214,47 +214,71 @@ class ExpertSet:
         return ExpertSet(**f)
 
 
+def _draw_expert(fmt: int, H: int, I: int, seed, e: int, device, std: float, tag: str):
+    """Expert e of a set, drawn from its own seed and encoded: a dict of
+    per-expert tensors (w13, w2 and the format's scales)."""
+    g = _gen(device, tag, seed, e, "w13")
+    w13 = torch.randn(2 * I, H, generator=g, device=device) * std
+    g = _gen(device, tag, seed, e, "w2")
+    w2 = torch.randn(H, I, generator=g, device=device) * std
+    if fmt == FMT_BF16:
+        return {"w13": w13.to(torch.bfloat16), "w2": w2.to(torch.bfloat16)}
+    if fmt == FMT_NVFP4:
+        q13, s13, g13 = encode_nvfp4(w13)
+        q2, s2, g2 = encode_nvfp4(w2)
+        return {"w13": q13, "w13_scale": s13, "w13_gscale": g13, "w2": q2, "w2_scale": s2, "w2_gscale": g2}
+    if fmt == FMT_FP8_B128:
+        q13, s13 = encode_fp8_b128(w13)
+        q2, s2 = encode_fp8_b128(w2)
+        return {"w13": q13, "w13_scale": s13, "w2": q2, "w2_scale": s2}
+    raise ValueError(f"unknown weight format {fmt}")
+
+
+def _empty_set(fmt: int, E: int, H: int, I: int, device) -> ExpertSet:
+    if fmt == FMT_BF16:
+        return ExpertSet(fmt, E, H, I, torch.zeros(E, 2 * I, H, dtype=torch.bfloat16, device=device),
+                         torch.zeros(E, H, I, dtype=torch.bfloat16, device=device))
+    if fmt == FMT_NVFP4:
+        return ExpertSet(fmt, E, H, I,
+                         torch.zeros(E, 2 * I, H // 2, dtype=torch.uint8, device=device),
+                         torch.zeros(E, H, I // 2, dtype=torch.uint8, device=device),
+                         torch.zeros(E, 2 * I, H // 16, dtype=torch.uint8, device=device),
+                         torch.zeros(E, H, I // 16, dtype=torch.uint8, device=device),
+                         torch.zeros(E, dtype=torch.float32, device=device),
+                         torch.zeros(E, dtype=torch.float32, device=device))
+    if fmt == FMT_FP8_B128:
+        return ExpertSet(fmt, E, H, I,
+                         torch.zeros(E, 2 * I, H, dtype=torch.uint8, device=device),
+                         torch.zeros(E, H, I, dtype=torch.uint8, device=device),
+                         torch.ones(E, 2 * I // 128, H // 128, dtype=torch.float32, device=device),
+                         torch.ones(E, H // 128, I // 128, dtype=torch.float32, device=device))
+    raise ValueError(f"unknown weight format {fmt}")
+
+
 def make_experts(fmt: int, E: int, H: int, I: int, seed, device="cpu", std: float = 0.02,
                  tag: str = "routed", only=None) -> ExpertSet:
     """E SwiGLU experts, each drawn from its own seed (so a subset regenerates alike).
 
     only: if given, just those experts are drawn and the rest stay zero (tests
     that touch a few experts of a large set use it to save time)."""
+    es = _empty_set(fmt, E, H, I, device)
     todo = range(E) if only is None else sorted(set(int(e) for e in only))
-    if fmt == FMT_BF16:
-        w13 = torch.zeros(E, 2 * I, H, dtype=torch.bfloat16, device=device)
-        w2 = torch.zeros(E, H, I, dtype=torch.bfloat16, device=device)
-        for e in todo:
-            g = _gen(device, tag, seed, e, "w13")
-            w13[e] = (torch.randn(2 * I, H, generator=g, device=device) * std).to(torch.bfloat16)
-            g = _gen(device, tag, seed, e, "w2")
-            w2[e] = (torch.randn(H, I, generator=g, device=device) * std).to(torch.bfloat16)
-        return ExpertSet(fmt, E, H, I, w13, w2)
-    if fmt == FMT_NVFP4:
-        w13 = torch.zeros(E, 2 * I, H // 2, dtype=torch.uint8, device=device)
-        s13 = torch.zeros(E, 2 * I, H // 16, dtype=torch.uint8, device=device)
-        g13 = torch.zeros(E, dtype=torch.float32, device=device)
-        w2 = torch.zeros(E, H, I // 2, dtype=torch.uint8, device=device)
-        s2 = torch.zeros(E, H, I // 16, dtype=torch.uint8, device=device)
-        g2 = torch.zeros(E, dtype=torch.float32, device=device)
-        for e in todo:
-            g = _gen(device, tag, seed, e, "w13")
-            w13[e], s13[e], g13[e] = encode_nvfp4(torch.randn(2 * I, H, generator=g, device=device) * std)
-            g = _gen(device, tag, seed, e, "w2")
-            w2[e], s2[e], g2[e] = encode_nvfp4(torch.randn(H, I, generator=g, device=device) * std)
-        return ExpertSet(fmt, E, H, I, w13, w2, s13, s2, g13, g2)
-    if fmt == FMT_FP8_B128:
-        w13 = torch.zeros(E, 2 * I, H, dtype=torch.uint8, device=device)
-        s13 = torch.ones(E, 2 * I // 128, H // 128, dtype=torch.float32, device=device)
-        w2 = torch.zeros(E, H, I, dtype=torch.uint8, device=device)
-        s2 = torch.ones(E, H // 128, I // 128, dtype=torch.float32, device=device)
-        for e in todo:
-            g = _gen(device, tag, seed, e, "w13")
-            w13[e], s13[e] = encode_fp8_b128(torch.randn(2 * I, H, generator=g, device=device) * std)
-            g = _gen(device, tag, seed, e, "w2")
-            w2[e], s2[e] = encode_fp8_b128(torch.randn(H, I, generator=g, device=device) * std)
-        return ExpertSet(fmt, E, H, I, w13, w2, s13, s2)
-    raise ValueError(f"unknown weight format {fmt}")
+    for e in todo:
+        for k, v in _draw_expert(fmt, H, I, seed, e, device, std, tag).items():
+            getattr(es, k)[e] = v
+    return es
+
+
+def make_expert_subset(fmt: int, experts, H: int, I: int, seed, device="cpu", std: float = 0.02,
+                       tag: str = "routed") -> ExpertSet:
+    """The listed experts of a set, each drawn from the same seed as in
+    make_experts, stored compactly: position i holds expert experts[i]."""
+    experts = [int(e) for e in experts]
+    es = _empty_set(fmt, len(experts), H, I, device)
+    for i, e in enumerate(experts):
+        for k, v in _draw_expert(fmt, H, I, seed, e, device, std, tag).items():
+            getattr(es, k)[i] = v
+    return es
 
 
 @dataclasses.dataclass

@@ -68,6 +68,7 @@ def lib():
         _lib.oracle_group_table.argtypes = [p, i, i, i, ctypes.c_uint, p, p]
         _lib.oracle_moe_layer_rows.argtypes = [p, p, p, p, p, i, i, i, i, i, i, p, i, p, i]
         _lib.oracle_unfused_layer.argtypes = [p, p, p, p, p, i, i, i, i, i, i, p]
+        _lib.oracle_moe_layer_uses.argtypes = [p, p, p, p, p, i, i, i, i, i, i, p, i, p, i]
     return _lib
 
 
@@ -204,6 +205,22 @@ def moe_layer(x_bf16, ids, topk_w, routed: WeightSet, shared: WeightSet, T, H, I
     out = np.empty((len(rows), H), np.float64)
     rs, ss = routed.cstruct(), shared.cstruct()
     lib().oracle_moe_layer_rows(x.ctypes.data, ids.ctypes.data, w.ctypes.data, ctypes.byref(rs),
+                                ctypes.byref(ss), T, H, I, I_shared, E, K, rows.ctypes.data,
+                                len(rows), out.ctypes.data, int(threads))
+    return out
+
+
+def moe_layer_uses(x_bf16, ids, topk_w, routed: WeightSet, shared: WeightSet, T, H, I, I_shared, E, K,
+                   rows=None, threads=1) -> np.ndarray:
+    """moe_layer with the expert evaluations of each row run on separate
+    threads (bitwise equal to moe_layer)."""
+    x = _np(x_bf16, np.uint16).reshape(-1)
+    ids = _np(ids, np.int32).reshape(-1)
+    w = _np(topk_w, np.float32).reshape(-1)
+    rows = np.arange(T, dtype=np.int32) if rows is None else np.ascontiguousarray(rows, np.int32)
+    out = np.empty((len(rows), H), np.float64)
+    rs, ss = routed.cstruct(), shared.cstruct()
+    lib().oracle_moe_layer_uses(x.ctypes.data, ids.ctypes.data, w.ctypes.data, ctypes.byref(rs),
                                 ctypes.byref(ss), T, H, I, I_shared, E, K, rows.ctypes.data,
                                 len(rows), out.ctypes.data, int(threads))
     return out

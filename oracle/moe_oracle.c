@@ -301,6 +301,56 @@ void oracle_moe_layer_rows(const uint16_t *x_bf16, const int32_t *ids,
     }
 }
 
+/* The same result as oracle_moe_layer_rows, with the expert evaluations of
+ * the listed rows (each row's shared use and its K picks) spread over OpenMP
+ * threads, then each row summed in the same fixed order (x, shared, picks
+ * 0..K-1) with the same operations, so the two agree bit for bit. Only the
+ * scheduling differs: it lets one row's experts run in parallel. */
+void oracle_moe_layer_uses(const uint16_t *x_bf16, const int32_t *ids,
+                           const float *topk_w, const oracle_weights *routed,
+                           const oracle_weights *shared, int T, int H, int I,
+                           int I_shared, int E, int K, const int32_t *rows,
+                           int nrows, double *ref, int nthreads)
+{
+    int K1 = K + 1, nuse = nrows * K1;
+    double *Y = (double *)malloc(sizeof(double) * (size_t)(nuse > 0 ? nuse : 1) * (size_t)H);
+    (void)T;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads > 0 ? nthreads : 1)
+#else
+    (void)nthreads;
+#endif
+    for (int u = 0; u < nuse; ++u) {
+        int j = u / K1, q = u % K1, t = rows[j];
+        int mx = H > I ? H : I;
+        if (I_shared > mx) mx = I_shared;
+        double *x = (double *)malloc(sizeof(double) * (size_t)H);
+        double *row = (double *)malloc(sizeof(double) * (size_t)mx);
+        double *y = Y + (size_t)u * H;
+        for (int h = 0; h < H; ++h) x[h] = oracle_bf16(x_bf16[(size_t)t * H + h]);
+        if (q == 0) {
+            expert_ffn(shared, H, I_shared, 0, x, NULL, y, row);
+        } else {
+            int id = ids[t * K + q - 1];
+            if (id >= 0 && id < E) expert_ffn(routed, H, I, id, x, NULL, y, row);
+        }
+        free(x); free(row);
+    }
+    for (int j = 0; j < nrows; ++j) {
+        int t = rows[j];
+        double *out = ref + (size_t)j * H;
+        for (int h = 0; h < H; ++h) out[h] = oracle_bf16(x_bf16[(size_t)t * H + h]);
+        for (int h = 0; h < H; ++h) out[h] += Y[((size_t)j * K1) * H + h];
+        for (int p = 0; p < K; ++p) {
+            int id = ids[t * K + p];
+            if (id < 0 || id >= E) continue;
+            for (int h = 0; h < H; ++h)
+                out[h] += (double)topk_w[t * K + p] * Y[((size_t)j * K1 + 1 + p) * H + h];
+        }
+    }
+    free(Y);
+}
+
 /* The same layer as the four unfused launches the pages list, each over all
  * rows, with its result held in its own buffer as if written to HBM:
  *   1. routed MoE       R[t] = sum_p w[t,p] * R_{ids[t,p]}(x[t])

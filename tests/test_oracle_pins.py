@@ -270,6 +270,20 @@ def test_row_subset_matches_full_rows():
     assert np.array_equal(sub, full[[5, 0, 3]])
 
 
+def test_uses_in_parallel_equal_rows_bit_for_bit():
+    """The form that runs a row's expert evaluations on separate threads (the
+    one the reference arm times) is the row-by-row form, rescheduled."""
+    L = _small_layer(inputs.FMT_NVFP4, inputs.FMT_FP8_B128)
+    L.topk_ids[1, 0] = L.shape.E + 1  # an out-of-range pick adds nothing in both
+    s = L.shape
+    args = (L.x, L.topk_ids, L.topk_w, _ws(L.routed), _ws(L.shared), s.T, s.H, s.I, s.I_shared, s.E, s.K)
+    full = oracle.moe_layer(*args)
+    for threads in (1, 3):
+        assert np.array_equal(oracle.moe_layer_uses(*args, threads=threads), full)
+    rows = np.array([4, 1], np.int32)
+    assert np.array_equal(oracle.moe_layer_uses(*args, rows=rows, threads=2), full[rows])
+
+
 # ------------------------------------------------ negative controls
 
 
