@@ -69,6 +69,7 @@ def lib():
         _lib.oracle_moe_layer_rows.argtypes = [p, p, p, p, p, i, i, i, i, i, i, p, i, p, i]
         _lib.oracle_unfused_layer.argtypes = [p, p, p, p, p, i, i, i, i, i, i, p]
         _lib.oracle_moe_layer_uses.argtypes = [p, p, p, p, p, i, i, i, i, i, i, p, i, p, i]
+        _lib.oracle_route.argtypes = [p, p, p, i, i, i, i, d, i, p, p, p]
     return _lib
 
 
@@ -224,6 +225,22 @@ def moe_layer_uses(x_bf16, ids, topk_w, routed: WeightSet, shared: WeightSet, T,
                                 ctypes.byref(ss), T, H, I, I_shared, E, K, rows.ctypes.data,
                                 len(rows), out.ctypes.data, int(threads))
     return out
+
+
+def route(x_bf16, wr_bf16, bias_bf16, T, H, E, K, scale=1.0, renorm=True):
+    """The router: (ids int32 [T][K], weights fp64 [T][K], keys fp64 [T][E]).
+
+    x_bf16 [T][H] and wr_bf16 [E][H] as bf16 bits (or bf16 tensors), bias_bf16
+    [E] or None. See oracle_route in moe_oracle.c for the definition."""
+    x = _np(x_bf16, np.uint16).reshape(-1)
+    wr = _np(wr_bf16, np.uint16).reshape(-1)
+    b = None if bias_bf16 is None else _np(bias_bf16, np.uint16).reshape(-1)
+    ids = np.zeros((T, K), np.int32)
+    w = np.zeros((T, K), np.float64)
+    keys = np.zeros((T, E), np.float64)
+    lib().oracle_route(x.ctypes.data, wr.ctypes.data, None if b is None else b.ctypes.data, T, H, E, K,
+                       float(scale), int(bool(renorm)), ids.ctypes.data, w.ctypes.data, keys.ctypes.data)
+    return ids, w, keys
 
 
 def unfused_layer(x_bf16, ids, topk_w, routed: WeightSet, shared: WeightSet, T, H, I, I_shared, E, K):

@@ -261,6 +261,62 @@ int oracle_group_table(const int32_t *ids, int T, int K, int E, unsigned flags,
     return G;
 }
 
+/* ---- the router ------------------------------------------------------ */
+/*
+ * The routing front end that produces topk_ids / topk_w from the layer input.
+ * "Daily AI Hotspot 2026-08-21", section "Most Worth Your Attention Today"
+ * (the SGLang #32340 paragraph): the shared-expert fusion had to handle a bf16
+ * correction bias and a top-k that is not a power of two (top-6). PR #27
+ * "each expert once", "Reviewer notes": every CTA routes all rows itself and
+ * the tie order is unchanged. The pages give no scoring formula; the reading
+ * taken is the DeepSeek-V3 one, for row t and routed expert e:
+ *
+ *     logit[t,e] = sum_h x[t,h] * Wr[e,h]                (Wr bf16 [E][H])
+ *     s[t,e]     = 1 / (1 + exp(-logit[t,e]))            (sigmoid score)
+ *     key[t,e]   = s[t,e] + bias[e]                      (bias bf16 [E], or 0)
+ *     ids[t,:]   = the K experts of largest key, in decreasing key order;
+ *                  equal keys: the lower expert index first
+ *     w[t,p]     = scale * s[t,ids[t,p]] / sum_q s[t,ids[t,q]]   (renorm = 1)
+ *                  scale * s[t,ids[t,p]]                          (renorm = 0)
+ *
+ * Everything in fp64 from the bf16 inputs. keys_out (optional, [T][E]) gets
+ * the selection keys so a test can tell a near tie from a wrong pick.
+ */
+void oracle_route(const uint16_t *x_bf16, const uint16_t *wr_bf16, const uint16_t *bias_bf16,
+                  int T, int H, int E, int K, double scale, int renorm,
+                  int32_t *ids_out, double *w_out, double *keys_out)
+{
+    double *s = (double *)malloc(sizeof(double) * (size_t)(E > 0 ? E : 1));
+    double *key = (double *)malloc(sizeof(double) * (size_t)(E > 0 ? E : 1));
+    char *taken = (char *)malloc((size_t)(E > 0 ? E : 1));
+    for (int t = 0; t < T; ++t) {
+        for (int e = 0; e < E; ++e) {
+            double acc = 0.0;
+            for (int h = 0; h < H; ++h)
+                acc += oracle_bf16(x_bf16[(size_t)t * H + h]) * oracle_bf16(wr_bf16[(size_t)e * H + h]);
+            s[e] = 1.0 / (1.0 + exp(-acc));
+            key[e] = s[e] + (bias_bf16 ? oracle_bf16(bias_bf16[e]) : 0.0);
+            taken[e] = 0;
+            if (keys_out) keys_out[(size_t)t * E + e] = key[e];
+        }
+        /* K passes of "largest remaining key, lowest index among equals" */
+        double sum = 0.0;
+        for (int p = 0; p < K; ++p) {
+            int best = -1;
+            for (int e = 0; e < E; ++e)
+                if (!taken[e] && (best < 0 || key[e] > key[best])) best = e;
+            taken[best] = 1;
+            ids_out[t * K + p] = best;
+            sum += s[best];
+        }
+        for (int p = 0; p < K; ++p) {
+            double v = s[ids_out[t * K + p]];
+            w_out[t * K + p] = scale * (renorm ? v / sum : v);
+        }
+    }
+    free(s); free(key); free(taken);
+}
+
 /* ---- the layer ------------------------------------------------------ */
 
 /* ref[j][:] for the rows listed in rows[0..nrows), straight from the
