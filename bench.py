@@ -38,6 +38,10 @@ WORKLOADS = {
     "dsv3_t8": dict(T=8, routing="mtp"),
     "dsv3_t64": dict(T=64, routing="zipf"),
 }
+# sweep points beyond the metric's workloads: the T=1 layer with the router
+# (bf16 [E][H] gate, bf16 correction bias, top-8, renormalised, scale 2.5)
+# computed inside the same launch
+ROUTED = {"dsv3_t1_routed": dict(T=1)}
 N_COPIES = 4
 KERNEL_SOURCES = ["moe_layer_decode_persistent_b300/csrc/api.cu",
                   "moe_layer_decode_persistent_b300/csrc/fused_fma.cuh",
@@ -286,7 +290,8 @@ def run_ours(args, rank, world, local):
     graph_us = graph_us_per_launch(launch_s, 4 * len(weights))
     assert B.moe_read_error(ws) == 0
 
-    # the other workloads of the metric (T=8, T=64), unless --no-sweep
+    # the other workloads of the metric (T=8, T=64) and the routed T=1 layer,
+    # unless --no-sweep
     del copies, weights
     torch.cuda.empty_cache()
     sweep = {}
@@ -295,6 +300,8 @@ def run_ours(args, rank, world, local):
             if name == args.workload:
                 continue
             sweep[name] = sweep_point(name, args, dev)
+        for name in ROUTED:
+            sweep[name] = routed_point(name, args, dev)
     wide = wide_sweep(args, dev) if args.sweep_wide else {}
     clk.__exit__()
     return dict(us_launch=us_launch_max, ms_per_step=ms_per_step, algo_bytes=algo_bytes,
@@ -376,6 +383,65 @@ def sweep_point(name, args, dev):
             "frac": round(gbs / peak, 4), "frac_graph": round(b / (g_us * 1e-6) / 1e9 / peak, 4),
             "distinct_experts": distinct, "algo_bytes": b, "launches": n, "T": wl["T"],
             "routing": wl["routing"]}
+
+
+def routed_point(name, args, dev):
+    """us per launch of the layer with its router inside the launch
+    (moe_fused_decode_routed): the same protocol as sweep_point. Every routed
+    expert's weights are drawn, since the router picks them."""
+    import torch
+
+    from moe_layer_decode_persistent_b300 import binding as B
+    from moe_layer_decode_persistent_b300 import inputs
+    T = ROUTED[name]["T"]
+    shape = inputs.dsv3(T, E=args.experts)
+    L = inputs.make_layer(shape, "uniform", 0, dev, inputs.FMT_NVFP4, inputs.FMT_FP8_B128)
+    g = torch.Generator(device=dev)
+    g.manual_seed(1234)
+    wr = (torch.randn(shape.E, shape.H, generator=g, device=dev) * (1.5 / shape.H ** 0.5)).to(torch.bfloat16)
+    bias = (torch.randn(shape.E, generator=g, device=dev) * 0.05).to(torch.bfloat16)
+    router = B.make_router(wr, bias, 2.5, True)
+    copies = [(L.routed, L.shared)] + [
+        (inputs.ExpertSet(**{k: (v.clone() if isinstance(v, torch.Tensor) else v)
+                             for k, v in L.routed.__dict__.items()}), L.shared)
+        for _ in range(N_COPIES - 1)]
+    weights = [(B.make_weights(r), B.make_weights(s)) for r, s in copies]
+    sh = B.make_shape(T, shape.H, shape.I, shape.I_shared, shape.E, shape.K, args.flags)
+    ws = torch.empty(B.moe_workspace_bytes(sh), dtype=torch.uint8, device=dev)
+    B.moe_workspace_init(ws)
+    out = torch.empty(T, shape.H, dtype=torch.bfloat16, device=dev)
+    ids = torch.empty(T, shape.K, dtype=torch.int32, device=dev)
+    tw = torch.empty(T, shape.K, dtype=torch.float32, device=dev)
+
+    def launch_s(i, s_=None):
+        rw, sw = weights[i % N_COPIES]
+        B.moe_fused_decode_routed(L.x, router, rw, sw, out, sh, ws, topk_ids=ids, topk_w=tw, stream=s_)
+
+    for i in range(3):
+        launch_s(i)
+    n = max(20, args.steps // 2)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    torch.cuda.synchronize()
+    for i in range(n):
+        ev[i][0].record()
+        launch_s(i)
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    assert B.moe_read_error(ws) == 0
+    us = statistics.mean(a.elapsed_time(b) * 1e3 for a, b in ev)
+    g_us = graph_us_per_launch(launch_s, 2 * N_COPIES)
+    assert B.moe_read_error(ws) == 0
+    distinct = len(set(ids.cpu().reshape(-1).tolist()))
+    b = (distinct * L.routed.nbytes_expert() + L.shared.nbytes_expert() + wr.numel() * 2 + bias.numel() * 2
+         + 2 * T * shape.H * 2 + T * shape.K * 8)
+    peak, _ = measured_peaks()
+    gbs = b / (us * 1e-6) / 1e9
+    del L, copies, weights
+    torch.cuda.empty_cache()
+    return {"us_per_launch": round(us, 2), "graph_us_per_launch": round(g_us, 2), "hbm_gbs": round(gbs, 1),
+            "frac": round(gbs / peak, 4), "frac_graph": round(b / (g_us * 1e-6) / 1e9 / peak, 4),
+            "distinct_experts": distinct, "algo_bytes": b, "launches": n, "T": T,
+            "routing": "router inside the launch (sigmoid + bf16 correction bias, top-8, renormalised)"}
 
 
 WIDE_T = [1, 2, 4, 8, 16, 32, 64, 128, 256]

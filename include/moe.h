@@ -226,6 +226,59 @@ moe_status moe_fused_decode_noalloc(const void *x, const int32_t *topk_ids,
                                     const moe_shape *s, uint32_t *err_out,
                                     void *stream);
 
+/*
+ * The routing front end: topk_ids and topk_w computed from the layer input.
+ * "Daily AI Hotspot 2026-08-21", section "Most Worth Your Attention Today"
+ * (the SGLang #32340 paragraph): a bf16 correction bias and a top-k whose K is
+ * not a power of two. PR #27 "each expert once", "Reviewer notes": every CTA
+ * routes all rows itself and the tie order is unchanged. The pages give no
+ * scoring formula; this library takes the DeepSeek-V3 one. For row t, expert e:
+ *
+ *   logit[t,e] = x[t] . wr[e]                 (fp32 sums of the bf16 products)
+ *   s[t,e]     = 1 / (1 + exp(-logit[t,e]))   (sigmoid score)
+ *   key[t,e]   = s[t,e] + bias[e]             (selection only)
+ *   topk_ids   = the K experts of largest key, largest first; equal keys: the
+ *                lower expert first
+ *   topk_w[p]  = scale * s[ids[p]] / sum_q s[ids[q]]   (renorm = 1)
+ *                scale * s[ids[p]]                     (renorm = 0)
+ *
+ *   wr    bf16 [E][H], H contiguous, 16-byte aligned (device)
+ *   bias  bf16 [E] correction bias (device), or NULL for none
+ * E <= 1024. The logits are summed in a fixed order, so the picks are the
+ * same on every call; keys that differ by less than the fp32 rounding of the
+ * logits may order differently from an exact computation.
+ */
+typedef struct {
+    const void *wr;
+    const void *bias;
+    float scale;
+    int renorm;
+} moe_router;
+
+/*
+ * The router alone (one cooperative launch): writes topk_ids int32 [T][K] and
+ * topk_w fp32 [T][K] (device). workspace as for moe_fused_decode
+ * (>= moe_workspace_bytes(s), initialised once).
+ */
+moe_status moe_route(const void *x, const moe_router *router, int32_t *topk_ids,
+                     float *topk_w, const moe_shape *s, void *workspace,
+                     size_t workspace_bytes, void *stream);
+
+/*
+ * The fused layer with the router inside the same launch: every CTA computes
+ * its share of the router's logits, waits for all of them, picks every row's
+ * experts on chip and builds its group table from them; the rest is
+ * moe_fused_decode with those picks and weights (bit for bit the result of
+ * moe_fused_decode given the topk_ids / topk_w this call returns).
+ *   topk_ids, topk_w  optional device outputs [T][K] (NULL to skip)
+ * Other arguments as for moe_fused_decode.
+ */
+moe_status moe_fused_decode_routed(const void *x, const moe_router *router,
+                                   const moe_weights *routed, const moe_weights *shared,
+                                   void *out, int32_t *topk_ids, float *topk_w,
+                                   const moe_shape *s, void *workspace,
+                                   size_t workspace_bytes, void *stream);
+
 /* Synchronise `stream`, copy the device error word to *err_bits and clear it. */
 moe_status moe_read_error(void *workspace, uint32_t *err_bits, void *stream);
 

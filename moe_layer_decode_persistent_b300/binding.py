@@ -21,14 +21,19 @@ MOE_W_BF16, MOE_W_NVFP4, MOE_W_FP8_B128 = 0, 1, 2
 # every symbol include/moe.h declares
 EXPORTS = ("moe_workspace_bytes", "moe_workspace_bytes_host", "moe_workspace_init",
            "moe_group_table_ints", "moe_group_table", "moe_fused_decode", "moe_fused_decode_host",
-           "moe_fused_decode_noalloc", "moe_read_error", "moe_status_string",
-           "moe_last_error_detail")
+           "moe_fused_decode_noalloc", "moe_route", "moe_fused_decode_routed", "moe_read_error",
+           "moe_status_string", "moe_last_error_detail")
 
 
 class moe_weights(ctypes.Structure):
     _fields_ = [("fmt", ctypes.c_int), ("w13", ctypes.c_void_p), ("w13_scale", ctypes.c_void_p),
                 ("w13_gscale", ctypes.c_void_p), ("w2", ctypes.c_void_p),
                 ("w2_scale", ctypes.c_void_p), ("w2_gscale", ctypes.c_void_p)]
+
+
+class moe_router(ctypes.Structure):
+    _fields_ = [("wr", ctypes.c_void_p), ("bias", ctypes.c_void_p), ("scale", ctypes.c_float),
+                ("renorm", ctypes.c_int)]
 
 
 class moe_shape(ctypes.Structure):
@@ -72,6 +77,11 @@ def lib():
         L.moe_fused_decode_host.argtypes = [P, P, P, wp, wp, P, sp, P, S, P]
         L.moe_fused_decode_noalloc.restype = I
         L.moe_fused_decode_noalloc.argtypes = [P, P, P, wp, wp, P, sp, P, P]
+        rp = ctypes.POINTER(moe_router)
+        L.moe_route.restype = I
+        L.moe_route.argtypes = [P, rp, P, P, sp, P, S, P]
+        L.moe_fused_decode_routed.restype = I
+        L.moe_fused_decode_routed.argtypes = [P, rp, wp, wp, P, P, P, sp, P, S, P]
         L.moe_read_error.restype = I
         L.moe_read_error.argtypes = [P, ctypes.POINTER(U), P]
         L.moe_status_string.restype = ctypes.c_char_p
@@ -165,6 +175,25 @@ def moe_fused_decode_noalloc(x, topk_ids, topk_w, routed: moe_weights, shared: m
     st = lib().moe_fused_decode_noalloc(_ptr(x), _ptr(topk_ids), _ptr(topk_w), ctypes.byref(routed),
                                         ctypes.byref(shared), _ptr(out), ctypes.byref(shape),
                                         _ptr(err_out), _stream(stream))
+    return _check(st) if check else st
+
+
+def make_router(wr, bias=None, scale=1.0, renorm=True) -> moe_router:
+    return moe_router(_ptr(wr), _ptr(bias), float(scale), int(bool(renorm)))
+
+
+def moe_route(x, router: moe_router, topk_ids, topk_w, shape: moe_shape, ws, stream=None, check=True):
+    st = lib().moe_route(_ptr(x), ctypes.byref(router), _ptr(topk_ids), _ptr(topk_w), ctypes.byref(shape),
+                         _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+    return _check(st) if check else st
+
+
+def moe_fused_decode_routed(x, router: moe_router, routed: moe_weights, shared: moe_weights, out,
+                            shape: moe_shape, ws, topk_ids=None, topk_w=None, stream=None, check=True):
+    st = lib().moe_fused_decode_routed(_ptr(x), ctypes.byref(router), ctypes.byref(routed),
+                                       ctypes.byref(shared), _ptr(out), _ptr(topk_ids), _ptr(topk_w),
+                                       ctypes.byref(shape), _ptr(ws), ws.numel() * ws.element_size(),
+                                       _stream(stream))
     return _check(st) if check else st
 
 

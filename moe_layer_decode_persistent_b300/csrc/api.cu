@@ -35,6 +35,7 @@ moe_status cuda_fail(cudaError_t e, const char *what) {
 
 constexpr int kMaxT = 256, kMaxK = 16, kMaxE = 1024, kMaxDim = 16384;
 static_assert(kMaxT * (kMaxK + 1) <= moe::kTcReadyCap, "group_ready capacity");
+static_assert(kMaxE <= moe::kRouterMaxE, "the router's picks hold every expert");
 static_assert(kMaxDim / 256 <= moe::kTcHtileCap, "htile_cnt capacity");
 static_assert(moe::group_table_scratch_ints(kMaxT, kMaxK, kMaxE) * 4 <= moe::kRawStageBytes,
               "the group table scratch fits in one raw stage");
@@ -55,6 +56,7 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 // never find their counters under another shape's scratch.
 constexpr size_t kTcTileCntWords = (size_t)moe::kSplitMaxT * (kMaxK + 1) * (kMaxDim / 128) * 4;
 struct WsLayout {
+    size_t route = 0;  // router partial logits [T][E][kRouterParts] fp32 (routed launches)
     size_t mid = 0, y = 0, fma_end = 0;
     size_t tc_ready = 0, tc_htile = 0, tc_tile = 0, tc_ctrl_end = 0, tc_P = 0, tc_Y = 0, tc_midB = 0,
            tc_xh = 0, tc_end = 0;
@@ -108,7 +110,9 @@ WsLayout ws_layout(const moe_shape *s) {
     off += T * H * 2;
     L.tc_end = align_up(off, 256);
 
-    L.dev_total = off = std::max(L.fma_end, L.tc_end);
+    L.route = off = std::max(L.fma_end, L.tc_end);
+    off = align_up(off + T * (size_t)std::max(s->E, 0) * moe::kRouterParts * sizeof(float), 256);
+    L.dev_total = off;
     L.st_x = off;
     off = align_up(off + T * H * 2, 256);
     L.st_ids = off;
@@ -178,8 +182,11 @@ moe::WeightsDev to_dev(const moe_weights *w) {
     return d;
 }
 
+// CUDA-core kernel and standalone table: the table, its scratch, then the
+// routed weights [T][K] (used by routed launches)
 size_t table_smem_bytes(const moe_shape *s) {
-    return sizeof(int32_t) * (size_t)(moe::group_table_ints(s->T, s->K) + moe::group_table_scratch_ints(s->T, s->K, s->E));
+    return sizeof(int32_t) * (size_t)(moe::group_table_ints(s->T, s->K) + moe::group_table_scratch_ints(s->T, s->K, s->E) +
+                                      s->T * s->K);
 }
 
 struct DevInfo {
@@ -215,7 +222,7 @@ moe_status dev_info(int dev, DevInfo *out) {
         e = cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
         if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(smem)");
         cudaFuncAttributes fa;
-        e = cudaFuncGetAttributes(&fa, moe::fused_tc_kernel<false>);
+        e = cudaFuncGetAttributes(&fa, moe::fused_tc_kernel<false, false>);
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncGetAttributes");
         d.tc_static_smem = (int)fa.sharedSizeBytes;
         g_dev[dev] = d;
@@ -464,6 +471,19 @@ moe_status launch_fused_tc(const moe::FusedParams &fp, const WsLayout &L, const 
     p.xh = reinterpret_cast<__half *>(ws + L.tc_xh);
     p.Ucap = s->T * (s->K + 1);
     p.Imax = std::max(s->I, s->I_shared);
+    p.route_mode = fp.route_mode;
+    p.router = fp.router;
+    for (int i = 0; i < 2; ++i) {  // 0: shared expert, 1: routed experts
+        const int fmt = i == 0 ? shared->fmt : routed->fmt, Ig = i == 0 ? s->I_shared : s->I;
+        moe::TcFmt &f = p.fc[i];
+        f.nt = moe::tc_nt(fmt, s->T);
+        f.nt_shift = f.nt == 32 ? 5 : 4;
+        f.tiles = Ig / 128;
+        f.nkc_gu = moe::tc_nkc_gu(fmt, s->H, s->T);
+        f.kc_gu = moe::tc_kc_gu(fmt, s->H, s->T);
+        f.nkc_dn = moe::tc_nkc_dn(Ig, s->T);
+        f.kc_dn = moe::tc_kc_dn(Ig, s->T);
+    }
     // the raw weight ring gets as many stages as shared memory holds
     const int smem_limit = d.max_smem_optin - d.tc_static_smem;
     const bool nd = (s->flags & MOE_FLAG_NO_DEDUP) != 0;
@@ -473,7 +493,9 @@ moe_status launch_fused_tc(const moe::FusedParams &fp, const WsLayout &L, const 
     const size_t smem = (size_t)moe::tc_smem_bytes(s->T, s->K, s->E, nd, nR);
     int occ = 0;
     const bool capped = moe::tc_capped_tables(s->T);
-    auto kern = capped ? moe::fused_tc_kernel<true> : moe::fused_tc_kernel<false>;
+    void (*kern)(const moe::TcParams) =
+        p.route_mode ? (capped ? moe::fused_tc_kernel<true, true> : moe::fused_tc_kernel<false, true>)
+                     : (capped ? moe::fused_tc_kernel<true, false> : moe::fused_tc_kernel<false, false>);
     if ((st = plan_occupancy(kern, dev, moe::kTcThreads, smem, d, &occ)) != MOE_OK) return st;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)d.nsm);  // one CTA per SM: it holds all of TMEM
@@ -503,14 +525,40 @@ size_t fma_compact_layout(const moe_shape *s, size_t *mid, size_t *y) {
 
 // fma_compact: the caller's buffer serves the CUDA-core kernel alone (the
 // no-allocation entry), with its scratch laid out by fma_compact_layout.
+moe_status check_router(const moe_router *r, const moe_shape *s) {
+    if (!r) return fail(MOE_ERR_INVALID_ARG, "router struct is NULL");
+    if (!r->wr) return fail(MOE_ERR_INVALID_ARG, "router weights are NULL");
+    if (!aligned(r->wr, 16)) return fail(MOE_ERR_INVALID_ARG, "router weights not 16-byte aligned");
+    if (r->bias && !aligned(r->bias, 2)) return fail(MOE_ERR_INVALID_ARG, "router bias not 2-byte aligned");
+    if (!(r->scale == r->scale)) return fail(MOE_ERR_INVALID_ARG, "router scale is NaN");
+    if (s->E > moe::kRouterMaxE) return fail(MOE_ERR_UNSUPPORTED, "the router handles E <= %d", moe::kRouterMaxE);
+    return MOE_OK;
+}
+
+moe::RouterDev router_dev(const moe_router *r, const WsLayout &L, void *ws, int32_t *ids_out, float *w_out) {
+    moe::RouterDev d;
+    d.wr = static_cast<const __nv_bfloat16 *>(r->wr);
+    d.bias = static_cast<const __nv_bfloat16 *>(r->bias);
+    d.scale = r->scale;
+    d.renorm = r->renorm ? 1 : 0;
+    d.part = reinterpret_cast<float *>(static_cast<char *>(ws) + L.route);
+    d.ids_out = ids_out;
+    d.w_out = w_out;
+    return d;
+}
+
+// router != null: a routed launch (the picks and weights come from the router
+// inside the launch; ids and w are ignored, ids_out / w_out receive them).
 moe_status fused_decode_impl(const void *x, const int32_t *ids, const float *w,
                              const moe_weights *routed, const moe_weights *shared, void *out,
                              const moe_shape *s, void *ws, size_t ws_bytes, cudaStream_t stream,
-                             bool fma_compact = false) {
+                             bool fma_compact = false, const moe_router *router = nullptr,
+                             int32_t *ids_out = nullptr, float *w_out = nullptr) {
     moe_status st = check_shape(s);
     if (st != MOE_OK) return st;
     if ((st = check_weights(routed, "routed")) != MOE_OK) return st;
     if ((st = check_weights(shared, "shared")) != MOE_OK) return st;
+    if (router && (st = check_router(router, s)) != MOE_OK) return st;
     if (!ws) return fail(MOE_ERR_INVALID_ARG, "workspace is NULL");
     if (!aligned(ws, 256)) return fail(MOE_ERR_INVALID_ARG, "workspace not 256-byte aligned");
     // host-only checks first: nothing below them touches the device until
@@ -519,14 +567,15 @@ moe_status fused_decode_impl(const void *x, const int32_t *ids, const float *w,
     size_t mid_off = L.mid, y_off = L.y, fma_need = L.fma_end;
     if (fma_compact) fma_need = fma_compact_layout(s, &mid_off, &y_off);
     const bool force_fma = fma_compact || (s->flags & MOE_FLAG_FORCE_FMA);
-    const size_t need_min = force_fma ? fma_need : std::min(fma_need, L.tc_end);
+    size_t need_min = force_fma ? fma_need : std::min(fma_need, L.tc_end);
+    if (router) need_min = L.dev_total;  // the router's partial logits sit past both paths' scratch
     if (ws_bytes < need_min)
         return fail(MOE_ERR_WORKSPACE, "workspace has %zu B, needs %zu B", ws_bytes, need_min);
     if (s->T == 0) return MOE_OK;
-    if (!x || !out || !ids || !w) return fail(MOE_ERR_INVALID_ARG, "NULL x/out/topk_ids/topk_w");
+    if (!x || !out || (!router && (!ids || !w))) return fail(MOE_ERR_INVALID_ARG, "NULL x/out/topk_ids/topk_w");
     if (!aligned(x, 16) || !aligned(out, 16))
         return fail(MOE_ERR_INVALID_ARG, "x and out must be 16-byte aligned");
-    if (!aligned(ids, 4) || !aligned(w, 4))
+    if (!aligned(router ? ids_out : ids, 4) || !aligned(router ? w_out : w, 4))
         return fail(MOE_ERR_INVALID_ARG, "topk_ids and topk_w must be 4-byte aligned");
     const size_t act_bytes = (size_t)s->T * s->H * 2;
     const uintptr_t xa = (uintptr_t)x, oa = (uintptr_t)out;
@@ -542,7 +591,7 @@ moe_status fused_decode_impl(const void *x, const int32_t *ids, const float *w,
     bool use_tc = tc_ok && !(s->flags & MOE_FLAG_FORCE_FMA);
     if ((s->flags & MOE_FLAG_FORCE_MMA) && !tc_ok)
         return fail(MOE_ERR_UNSUPPORTED, "tensor-core path requested but unavailable: %s", why);
-    const size_t need = use_tc ? L.tc_end : fma_need;
+    const size_t need = router ? L.dev_total : use_tc ? L.tc_end : fma_need;
     if (ws_bytes < need)
         return fail(MOE_ERR_WORKSPACE, "workspace has %zu B, needs %zu B", ws_bytes, need);
 
@@ -564,6 +613,9 @@ moe_status fused_decode_impl(const void *x, const int32_t *ids, const float *w,
     p.mid = reinterpret_cast<float *>(static_cast<char *>(ws) + mid_off);
     p.y = reinterpret_cast<float *>(static_cast<char *>(ws) + y_off);
     p.Imax = std::max(s->I, s->I_shared);
+    p.route_mode = router ? 1 : 0;
+    memset(&p.router, 0, sizeof p.router);
+    if (router) p.router = router_dev(router, L, ws, ids_out, w_out);
     if (use_tc) return launch_fused_tc(p, L, s, routed, shared, dev, d, stream);
     return launch_fused_fma(p, s, dev, d, stream);
 }
@@ -705,6 +757,53 @@ moe_status moe_fused_decode(const void *x, const int32_t *topk_ids, const float 
                             void *stream) {
     return fused_decode_impl(x, topk_ids, topk_w, routed, shared, out, s, workspace,
                              workspace_bytes, (cudaStream_t)stream);
+}
+
+moe_status moe_route(const void *x, const moe_router *router, int32_t *topk_ids, float *topk_w,
+                     const moe_shape *s, void *workspace, size_t workspace_bytes, void *stream) {
+    moe_status st = check_shape(s);
+    if (st != MOE_OK) return st;
+    if ((st = check_router(router, s)) != MOE_OK) return st;
+    if (!workspace) return fail(MOE_ERR_INVALID_ARG, "workspace is NULL");
+    if (!aligned(workspace, 256)) return fail(MOE_ERR_INVALID_ARG, "workspace not 256-byte aligned");
+    const WsLayout L = ws_layout(s);
+    if (workspace_bytes < L.dev_total)
+        return fail(MOE_ERR_WORKSPACE, "workspace has %zu B, needs %zu B", workspace_bytes, L.dev_total);
+    if (s->T == 0) return MOE_OK;
+    if (!x || !topk_ids || !topk_w) return fail(MOE_ERR_INVALID_ARG, "NULL x/topk_ids/topk_w");
+    if (!aligned(x, 16)) return fail(MOE_ERR_INVALID_ARG, "x must be 16-byte aligned");
+    if (!aligned(topk_ids, 4) || !aligned(topk_w, 4))
+        return fail(MOE_ERR_INVALID_ARG, "topk_ids and topk_w must be 4-byte aligned");
+    int dev = 0;
+    if ((st = current_device(&dev)) != MOE_OK) return st;
+    DevInfo d;
+    if ((st = dev_info(dev, &d)) != MOE_OK) return st;
+    int occ = 0;
+    if ((st = plan_occupancy(moe::route_kernel, dev, 256, 0, d, &occ)) != MOE_OK) return st;
+    moe::RouterDev r = router_dev(router, L, workspace, topk_ids, topk_w);
+    const __nv_bfloat16 *xb = static_cast<const __nv_bfloat16 *>(x);
+    moe::WsHeader *hdr = static_cast<moe::WsHeader *>(workspace);
+    int T = s->T, H = s->H, E = s->E, K = s->K;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(d.nsm * occ));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = (cudaStream_t)stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, moe::route_kernel, xb, r, T, H, E, K, hdr);
+    if (e != cudaSuccess) return cuda_fail(e, "launch route_kernel");
+    return MOE_OK;
+}
+
+moe_status moe_fused_decode_routed(const void *x, const moe_router *router, const moe_weights *routed,
+                                   const moe_weights *shared, void *out, int32_t *topk_ids, float *topk_w,
+                                   const moe_shape *s, void *workspace, size_t workspace_bytes, void *stream) {
+    return fused_decode_impl(x, nullptr, nullptr, routed, shared, out, s, workspace, workspace_bytes,
+                             (cudaStream_t)stream, false, router, topk_ids, topk_w);
 }
 
 moe_status moe_fused_decode_host(const void *x_host, const int32_t *ids_host, const float *w_host,

@@ -24,6 +24,7 @@
 
 #include "group_table.cuh"
 #include "moe_common.cuh"
+#include "router.cuh"
 
 namespace moe {
 
@@ -39,6 +40,8 @@ struct FusedParams {
     float *mid;  // [Ucap][Imax]
     float *y;    // [Ucap][H]
     int Imax;
+    int route_mode;  // 1: the picks and weights come from the router below, not ids/topk_w
+    RouterDev router;
 };
 
 constexpr int kFmaThreads = 256;
@@ -210,15 +213,27 @@ __global__ void __launch_bounds__(kFmaThreads) fused_fma_kernel(FusedParams p) {
     const bool no_dedup = (p.flags & kFlagNoDedup) != 0;
     GroupTable tab{tbl, T * (K + 1), T * (K + 1)};
     int *scr = tbl + group_table_ints(T, K);
-    group_table_cta(p.ids, T, K, p.E, no_dedup, tab, scr, blockIdx.x == 0 ? &p.hdr->err : nullptr);
-
-    const int G = tab.G();
-    const int32_t *gexp = tab.gexp(), *gn = tab.gncols(), *g0 = tab.gcol0(),
-                  *crow = tab.col_row(), *rcol = tab.row_col();
+    float *tw_s = reinterpret_cast<float *>(scr + group_table_scratch_ints(T, K, p.E));  // [T][K] routed weights
     const int lane = threadIdx.x & 31;
     const int nwarps_cta = blockDim.x >> 5;
     const int gw = blockIdx.x * nwarps_cta + (threadIdx.x >> 5);
     const int nw = gridDim.x * nwarps_cta;
+
+    // ---- phase R (routed launches): partial logits over every warp of the
+    // grid, then each CTA picks every row's experts on chip ----------------
+    if (p.route_mode) {
+        router_logits(p.router, p.x, T, H, p.E, gw, nw);
+        if (!grid_barrier(p.hdr, gridDim.x, false)) return;
+        router_picks(p.router, T, p.E, K, threadIdx.x >> 5, nwarps_cta, group_table_picks(scr, p.E), tw_s, K,
+                     blockIdx.x == 0);
+    }
+    group_table_cta(p.route_mode ? nullptr : p.ids, T, K, p.E, no_dedup, tab, scr,
+                    blockIdx.x == 0 ? &p.hdr->err : nullptr, 0, blockDim.x, 0);
+    const float *topk_w = p.route_mode ? tw_s : p.topk_w;
+
+    const int G = tab.G();
+    const int32_t *gexp = tab.gexp(), *gn = tab.gncols(), *g0 = tab.gcol0(),
+                  *crow = tab.col_row(), *rcol = tab.row_col();
     const int n_shared_groups = no_dedup ? T : (T > 0 ? 1 : 0);
 
     // ---- phase A: gate/up + SwiGLU --------------------------------------
@@ -292,7 +307,7 @@ __global__ void __launch_bounds__(kFmaThreads) fused_fma_kernel(FusedParams p) {
             acc = __fadd_rn(acc, __ldcg(p.y + (size_t)rc[0] * H + h));
             for (int q = 0; q < K; ++q) {
                 const int c = rc[1 + q];
-                if (c >= 0) acc = __fmaf_rn(p.topk_w[t * K + q], __ldcg(p.y + (size_t)c * H + h), acc);
+                if (c >= 0) acc = __fmaf_rn(topk_w[t * K + q], __ldcg(p.y + (size_t)c * H + h), acc);
             }
             p.out[idx] = __float2bfloat16_rn(acc);
         }
@@ -307,7 +322,7 @@ __global__ void __launch_bounds__(256) group_table_kernel(const int32_t *ids, in
     int32_t *tbl = reinterpret_cast<int32_t *>(smem_i4);
     GroupTable tab{tbl, T * (K + 1), T * (K + 1)};
     int *scr = tbl + group_table_ints(T, K);
-    group_table_cta(ids, T, K, E, (flags & kFlagNoDedup) != 0, tab, scr, err_word);
+    group_table_cta(ids, T, K, E, (flags & kFlagNoDedup) != 0, tab, scr, err_word, 0, blockDim.x, 0);
     for (int i = threadIdx.x; i < group_table_ints(T, K); i += blockDim.x) out[i] = tbl[i];
 }
 

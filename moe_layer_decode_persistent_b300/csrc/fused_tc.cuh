@@ -61,6 +61,7 @@
 
 #include "group_table.cuh"
 #include "moe_common.cuh"
+#include "router.cuh"
 #include "sm100.cuh"
 
 namespace moe {
@@ -108,6 +109,16 @@ struct TcMaps {
     CUtensorMap r13, r13s, r2, r2s, s13, s13s, s2, s2s;
 };
 
+// Job-list constants of one expert set (index 0: the shared expert, 1: the
+// routed experts), fixed by the launch's shape and computed on the host, so
+// the per-group bookkeeping at the start of a launch needs no division.
+struct TcFmt {
+    int nt, nt_shift;  // columns per job and log2 of it
+    int tiles;         // 128-row tiles of the intermediate (Ig / 128)
+    int nkc_gu, kc_gu; // gate/up K chunks and their length
+    int nkc_dn, kc_dn; // down K chunks and their length
+};
+
 struct TcParams {
     TcMaps maps;
     const __nv_bfloat16 *x;
@@ -127,6 +138,9 @@ struct TcParams {
     uint8_t *midB;          // f16 intermediate in MMA B layout
     __half *xh;             // the activations as f16 [T][H]
     int Ucap, Imax;
+    int route_mode;         // 1: the picks and weights come from the router, not ids/topk_w
+    RouterDev router;
+    TcFmt fc[2];            // 0: shared expert, 1: routed experts
 };
 
 struct TcJob {
@@ -176,8 +190,8 @@ struct TcSmem {
     static constexpr int bbuf = 0;
     static constexpr int jobs = bbuf + kASlotsMax * kBUnitBytes;
     static constexpr int bars = jobs + kJobSlots * (int)sizeof(TcJob);
-    // jfull, jempty, rfull, rempty, sfull, sempty, dfull, dempty, drain[4]
-    static constexpr int nbars = 2 * kJobSlots + 2 * kRawStagesMax + 2 * kASlotsMax + 2 * 2 + kIssuers;
+    // jfull, jempty, rfull, rempty, sfull, sempty, dfull, dempty, drain[4], coef
+    static constexpr int nbars = 2 * kJobSlots + 2 * kRawStagesMax + 2 * kASlotsMax + 2 * 2 + kIssuers + 1;
     static constexpr int misc = bars + nbars * 8;  // tmem addr, abort, down jobs per tile, parity
     static constexpr int tile_ready = misc + 64;   // per 256-row output tile: combine may start (64 max)
     static constexpr int tables = tile_ready + 256;  // group table, then per-group arrays
@@ -252,7 +266,10 @@ __device__ __forceinline__ void tc_convert_x(const TcParams &p, int gt, int nthr
     if (range_bad) atomicOr(&p.hdr->err, kErrRange);
 }
 
-template <bool kCappedTables>
+// kRouted: the picks and weights come from the router inside the launch (a
+// separate instantiation, so the router's registers never weigh on the
+// unrouted kernel's hot loops).
+template <bool kCappedTables, bool kRouted>
 __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_constant__ TcParams p) {
     using namespace sm100;
     extern __shared__ __align__(1024) uint8_t smem_raw_[];
@@ -275,6 +292,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
     uint64_t *sfull = rempty + kRawStagesMax, *sempty = sfull + kASlotsMax;
     uint64_t *dfull = sempty + kASlotsMax, *dempty = dfull + 2;
     uint64_t *drain = dempty + 2;
+    uint64_t *coef_bar = drain + kIssuers;  // the combine coefficients are filled
     uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(smem + TcSmem::misc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + TcSmem::misc + 4);
     int *dn_per_ht_s = reinterpret_cast<int *>(smem + TcSmem::misc + 8);
@@ -329,6 +347,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
             mbar_init(&dempty[i], 4);
         }
         for (int i = 0; i < kIssuers; ++i) mbar_init(&drain[i], 1);
+        mbar_init(coef_bar, 4);  // one arrival per epilogue warp
         for (int i = 0; i < 64; ++i) tile_ready_s[i] = 0;
         *abort_flag = 0;
         fence_mbar_init();
@@ -336,12 +355,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
         // first in the list, so when this CTA's first job (job b) is one of them
         // the shape alone defines it: its first stages stream in while the group
         // table is built (the table's scratch sits in the ring's last stage).
-        const int fmt0 = p.shared.fmt, nt0 = tc_nt(fmt0, T), n0 = no_dedup ? 1 : T;
-        const int tiles0 = p.Is / 128, nkc0 = tc_nkc_gu(fmt0, H, T), b = (int)blockIdx.x;
-        if (b < ((n0 + nt0 - 1) / nt0) * tiles0 * nkc0) {
+        const TcFmt &f0 = p.fc[0];
+        const int fmt0 = p.shared.fmt, n0 = no_dedup ? 1 : T;
+        const int tiles0 = f0.tiles, nkc0 = f0.nkc_gu, b = (int)blockIdx.x;
+        if (b < ((n0 + f0.nt - 1) >> f0.nt_shift) * tiles0 * nkc0) {
             fence_proxy_async_smem();
-            const int rem = b % (tiles0 * nkc0), tile = rem / nkc0, kc = rem - (rem / nkc0) * nkc0;
-            const int kc_len = tc_kc_gu(fmt0, H, T), k0 = kc * kc_len;
+            const int rem = b % (tiles0 * nkc0), tile = rem / nkc0, kc = rem - tile * nkc0;
+            const int kc_len = f0.kc_gu, k0 = kc * kc_len;
             const bool fp4 = fmt0 == kFmtNvfp4;
             const int nst = (min(kc_len, H - k0) / kUnitK) / (fp4 ? 2 : 1);
             npre = min(nst, nR - 1);
@@ -359,50 +379,102 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
         // result is used after the conversion's loads are in flight)
         if (lane == 0) start_no = atomicInc(&p.hdr->start_cnt, 2u * gridDim.x - 1u);
     }
+    int *gt_scr = reinterpret_cast<int *>(raw + (nR - 1) * kRawStageBytes);  // group table scratch
+    // The step's picks and router weights come first, in the same round trip
+    // as the activations and ahead of the weight stream: the picks into the
+    // group table's scratch, the weights into the pick slots of the combine
+    // weights (a routed launch computes both on chip below).
+    if (warp >= 1 && !kRouted) {
+        int32_t *picks = group_table_picks(gt_scr, p.E);
+        for (int j = tid - 32; j < T * K; j += nw1) {
+            const int t = j / K;
+            picks[j] = __ldg(p.ids + j);
+            comb_w[j + t + 1] = __ldg(p.topk_w + j);  // [t][1 + q]
+        }
+    }
     if (warp >= 1) tc_convert_x(p, (tid - 32) * (int)gridDim.x + (int)blockIdx.x, nw1 * (int)gridDim.x);
     if (tid == 32) *par_s = (int)(start_no / gridDim.x);
 
-    // group table (its scratch is the raw ring's last stage; it ends with a CTA
-    // barrier, which also publishes the barriers, the parity and the TMEM address)
-    group_table_cta(p.ids, T, K, p.E, no_dedup, tab, reinterpret_cast<int *>(raw + (nR - 1) * kRawStageBytes),
-                    blockIdx.x == 0 ? err : nullptr);
+    // routed launches: warps 1.. of every CTA compute their share of the
+    // router's partial logits (warp 0 streams the first weights meanwhile),
+    // then every CTA waits for all of them and picks every row's experts on
+    // chip: the picks go to the group table's scratch, the weights to the
+    // combine weights of the pick slots
+    if (kRouted && warp >= 1) {
+        const int ncw = kTcThreads / 32 - 1;
+        router_logits(p.router, p.x, T, H, p.E, (warp - 1) * (int)gridDim.x + (int)blockIdx.x,
+                      ncw * (int)gridDim.x);
+        named_bar_sync(2, nw1);
+        if (tid == 32) {
+            __threadfence();
+            uint32_t *rr = &p.hdr->route_ready[*par_s];
+            red_add_release_gpu(rr, 1u);
+            const unsigned long long t0 = globaltimer_ns();
+            while (ld_acquire_gpu(rr) < gridDim.x) {
+                if (globaltimer_ns() - t0 > kWaitBudgetNs) {
+                    atomicOr(err, kErrWaitTimeout);
+                    *abort_flag = 1;
+                    break;
+                }
+                __nanosleep(64);
+            }
+        }
+        named_bar_sync(2, nw1);
+        int32_t *picks = group_table_picks(gt_scr, p.E);
+        if (*abort_flag) {
+            for (int j = tid - 32; j < T * K; j += nw1) picks[j] = -1;
+        } else {
+            router_picks(p.router, T, p.E, K, warp - 1, ncw, picks, comb_w + 1, K + 1, blockIdx.x == 0);
+        }
+    }
+
+    // the group table, by warps 1.. behind named barrier 1 (warp 0 streams
+    // meanwhile; the table's scratch is the raw ring's last stage); then this
+    // CTA's slice of the activations is published, and one CTA barrier
+    // publishes the mbarriers, the TMEM address, the parity and the table
+    if (warp >= 1) {
+        group_table_cta(nullptr, T, K, p.E, no_dedup, tab, gt_scr, blockIdx.x == 0 ? err : nullptr, 32, nw1, 1);
+        if (tid == 32) {  // the table's barriers ordered this CTA's activation stores
+            __threadfence();
+            red_add_release_gpu(&p.hdr->x_ready[*par_s], 1u);
+        }
+    }
+    __syncthreads();
+    tc_fence_after();
     const int G = tab.G();
     const int32_t *gexp = tab.gexp(), *gn = tab.gncols(), *g0 = tab.gcol0(), *rcol = tab.row_col();
     const int *crow = tab.col_row();
     const int par = *par_s;
     uint32_t *group_ready = p.group_ready + par * kTcReadyCap;
     uint32_t *htile_cnt = p.htile_cnt + par * kTcHtileCap;
-    if (tid == 32) {  // this CTA's activation slice is converted (the table's barriers ordered it)
-        __threadfence();
-        red_add_release_gpu(&p.hdr->x_ready[par], 1u);
-    }
     if (warp == 0) {
-        int run[5] = {0, 0, 0, 0, 0};
+        // per-group job counts and their prefix sums, 32 groups per round:
+        // gate/up jobs, down jobs, (column tile, row tile) pairs, padded
+        // intermediate columns x row tiles, column tiles, and down jobs per
+        // 256-row output tile
+        int run[6] = {0, 0, 0, 0, 0, 0};
         for (int base = 0; base < G; base += 32) {
             const int g = base + lane;
-            int v[5] = {0, 0, 0, 0, 0};  // gu jobs, dn jobs, tiles, mid units, pairs
+            int v[6] = {0, 0, 0, 0, 0, 0};
             if (g < G) {
-                const bool sh = gexp[g] < 0;
-                const int fmt = sh ? p.shared.fmt : p.routed.fmt;
-                const int Ig = sh ? p.Is : p.I;
-                const int nt = tc_nt(fmt, T);
-                const int n = gn[g], nct = (n + nt - 1) / nt;
-                const int tiles = Ig / 128;
-                int np = 0;
-                for (int ct = 0; ct < nct; ++ct) np += ((min(nt, n - ct * nt) + 15) / 16) * 16;
-                v[0] = nct * tiles * tc_nkc_gu(fmt, H, T);
-                v[1] = nct * (H / 256) * tc_nkc_dn(Ig, T);
-                v[2] = nct * tiles;
-                v[3] = np * tiles;
+                const TcFmt &f = p.fc[gexp[g] < 0 ? 0 : 1];
+                const int n = gn[g], nct = (n + f.nt - 1) >> f.nt_shift;
+                const int last = n - (nct - 1) * f.nt;  // columns of the last column tile
+                const int np = (nct - 1) * f.nt + ((last + 15) & ~15);
+                v[0] = nct * f.tiles * f.nkc_gu;
+                v[1] = nct * (H >> 8) * f.nkc_dn;
+                v[2] = nct * f.tiles;
+                v[3] = np * f.tiles;
                 v[4] = nct;
+                v[5] = nct * f.nkc_dn;
             }
-            int sc[5];
+            int sc[6];
 #pragma unroll
-            for (int a = 0; a < 5; ++a) sc[a] = v[a];
+            for (int a = 0; a < 6; ++a) sc[a] = v[a];
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
 #pragma unroll
-                for (int a = 0; a < 5; ++a) {
+                for (int a = 0; a < 6; ++a) {
                     const int y = __shfl_up_sync(0xffffffffu, sc[a], o);
                     if (lane >= o) sc[a] += y;
                 }
@@ -415,7 +487,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                 pair_prefix[g] = run[4] + sc[4] - v[4];
             }
 #pragma unroll
-            for (int a = 0; a < 5; ++a) run[a] += __shfl_sync(0xffffffffu, sc[a], 31);
+            for (int a = 0; a < 6; ++a) run[a] += __shfl_sync(0xffffffffu, sc[a], 31);
         }
         if (lane == 0) {
             gu_prefix[G] = run[0];
@@ -423,14 +495,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
             tile_prefix[G] = run[2];
             mid_prefix[G] = run[3];
             pair_prefix[G] = run[4];
-            int dph_total = 0;  // down jobs that write one 256-row output tile
-            for (int g = 0; g < G; ++g) {
-                const bool sh = gexp[g] < 0;
-                const int nt = tc_nt(sh ? p.shared.fmt : p.routed.fmt, T);
-                dph_total += ((gn[g] + nt - 1) / nt) * tc_nkc_dn(sh ? p.Is : p.I, T);
-            }
-            // read by the other warps after their first job-slot wait
-            *dn_per_ht_s = dph_total;
+            // down jobs that write one 256-row output tile; read by the other
+            // warps after their first job-slot wait
+            *dn_per_ht_s = run[5];
         }
         __syncwarp();
     } else {
@@ -439,33 +506,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
         {
             const int opar = par ^ 1;
             const int gt = (int)blockIdx.x * nw1 + (tid - 32);
-            const int nz = kTcReadyCap + kTcHtileCap + 2;
+            const int nz = kTcReadyCap + kTcHtileCap + 3;
             for (int i = gt; i < nz; i += nw1 * (int)gridDim.x) {
                 if (i < kTcReadyCap) p.group_ready[opar * kTcReadyCap + i] = 0u;
                 else if (i < kTcReadyCap + kTcHtileCap) p.htile_cnt[opar * kTcHtileCap + i - kTcReadyCap] = 0u;
                 else if (i == kTcReadyCap + kTcHtileCap) p.hdr->job_next[opar] = 0u;
-                else p.hdr->x_ready[opar] = 0u;
+                else if (i == kTcReadyCap + kTcHtileCap + 1) p.hdr->x_ready[opar] = 0u;
+                else p.hdr->route_ready[opar] = 0u;
             }
         }
-        // combine coefficients of every (row, slot): weight 1 and the shared
-        // down scale for slot 0, the router weight and the expert's down scale
-        // for pick slots
-        for (int i = tid - 32; i < C; i += nw1) {
-            const int t = i / (K + 1), q = i - t * (K + 1);
-            float w = 1.0f, gsc = 1.0f;
-            if (q == 0) {
-                if (p.shared.fmt == kFmtNvfp4) gsc = __ldg(p.shared.w2_gscale);
-            } else {
-                w = __ldg(p.topk_w + t * K + q - 1);
-                const int c = rcol[i];
-                if (c >= 0 && p.routed.fmt == kFmtNvfp4)
-                    gsc = __ldg(p.routed.w2_gscale + gexp[group_of_col(g0, G, c)]);
-            }
-            comb_w[i] = w;
-            comb_g[i] = gsc;
-        }
-        named_bar_sync(1, nw1);  // the coefficients, among warps 1..
-        tc_fence_after();
     }
     const uint32_t tmem = *tmem_base_s;
 
@@ -501,35 +550,36 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                         local = jd - dn_prefix[g];
                     }
                     const bool sh = gexp[g] < 0;
+                    const TcFmt &f = p.fc[sh ? 0 : 1];
                     d.g = g;
                     d.shared = sh;
                     d.e = sh ? 0 : gexp[g];
                     d.fmt = sh ? p.shared.fmt : p.routed.fmt;
                     d.Ig = sh ? p.Is : p.I;
-                    const int tiles = d.Ig / 128;
-                    const int nt = tc_nt(d.fmt, T);
+                    const int tiles = f.tiles;
+                    const int nt = f.nt;
                     if (gu) {
                         d.kind = 0;
-                        d.nkc = tc_nkc_gu(d.fmt, H, T);
+                        d.nkc = f.nkc_gu;
                         const int per_ct = tiles * d.nkc;
                         d.ct = local / per_ct;
                         const int rem = local - d.ct * per_ct;
                         d.tile = rem / d.nkc;
                         d.kc = rem - d.tile * d.nkc;
-                        const int kc_len = tc_kc_gu(d.fmt, H, T);
+                        const int kc_len = f.kc_gu;
                         d.k0 = d.kc * kc_len;
                         d.nunits = min(kc_len, H - d.k0) / kUnitK;
                         d.rows0 = d.tile * 128;
                         d.rows1 = d.Ig + d.tile * 128;
                     } else {
                         d.kind = 1;
-                        d.nkc = tc_nkc_dn(d.Ig, T);
-                        const int per_ct = (H / 256) * d.nkc;
+                        d.nkc = f.nkc_dn;
+                        const int per_ct = (H >> 8) * d.nkc;
                         d.ct = local / per_ct;
                         const int rem = local - d.ct * per_ct;
                         d.tile = rem / d.nkc;
                         d.kc = rem - d.tile * d.nkc;
-                        const int kc_len = tc_kc_dn(d.Ig, T);
+                        const int kc_len = f.kc_dn;
                         d.k0 = d.kc * kc_len;
                         d.nunits = min(kc_len, d.Ig - d.k0) / kUnitK;
                         d.rows0 = d.tile * 256;
@@ -872,6 +922,28 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
         const int r = (quarter << 5) | lane;
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
         int js = 0, jph = 0, ds = 0, dph = 0;
+        // The combine coefficients of every (row, slot), filled here while
+        // the first MMAs are still ahead (the combine waits for coef_bar):
+        // weight 1 and the shared down scale for slot 0, the expert's down
+        // scale for pick slots (their router weights are in place already).
+        {
+            const int etid = (warp - 2 - kIssuers - kDqWarps) * 32 + lane;
+            for (int i = etid; i < C; i += 128) {
+                const int q = i % (K + 1);
+                float gsc = 1.0f;
+                if (q == 0) {
+                    comb_w[i] = 1.0f;
+                    if (p.shared.fmt == kFmtNvfp4) gsc = __ldg(p.shared.w2_gscale);
+                } else {
+                    const int c = rcol[i];
+                    if (c >= 0 && p.routed.fmt == kFmtNvfp4)
+                        gsc = __ldg(p.routed.w2_gscale + gexp[group_of_col(g0, G, c)]);
+                }
+                comb_g[i] = gsc;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(coef_bar);
+        }
         // fault injection (MOE_FLAG_DEBUG_DROP_ARRIVE): CTA 0's first quarter
         // skips its first intermediate-ready arrival, so the down jobs of that
         // (group, column tile) wait out their budget and the launch aborts
@@ -1095,7 +1167,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
             __nanosleep(128);
         }
         __syncwarp();
-    } else if (!*abort_flag) {
+    } else if (!*abort_flag && __all_sync(0xffffffffu, mbar_wait(coef_bar, 0, abort_flag, err))) {
         const int ncw = kTcThreads / 32 - 1, hw = H / 32;  // combine warps 1..
         const long long nwu = (long long)T * hw;
         const int nkc_s = tc_nkc_dn(p.Is, T), nkc_r = tc_nkc_dn(p.I, T);

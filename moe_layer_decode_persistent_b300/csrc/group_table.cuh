@@ -53,17 +53,29 @@ __host__ __device__ constexpr int group_capacity(int T, int K, int E, bool no_de
 // Shared-memory ints group_table_cta needs besides the table: three per-expert
 // arrays of E ints and a copy of the T*K picks.
 __host__ __device__ constexpr int group_table_scratch_ints(int T, int K, int E) { return 3 * E + T * K; }
+// Where in that scratch the copy of the picks ([T][K]) sits.
+__host__ __device__ inline int *group_table_picks(int *scr, int E) { return scr + 3 * E; }
 
 // Build the table for ids [T][K] into `tab` (shared memory) using `scr`
-// (shared, group_table_scratch_ints(T, K, E) ints). Whole CTA calls; ends with a
-// __syncthreads. Error bits are OR-ed into *err_word when err_word != null.
+// (shared, group_table_scratch_ints(T, K, E) ints). Error bits are OR-ed into
+// *err_word when err_word != null.
+// ids == null: the picks are already in the scratch's pick copy
+// (group_table_picks(scr, E)), put there by the on-chip router.
+// The participating threads are threadIdx.x in [tid0, tid0 + nthr) (whole
+// warps), synchronised with named barrier `bar` (bar 0 with the whole CTA is
+// __syncthreads); the last barrier leaves the table visible to them.
+__device__ __forceinline__ void gt_sync(int bar, int nthr) {
+    asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(nthr) : "memory");
+}
+
 __device__ void group_table_cta(const int32_t *__restrict__ ids, int T, int K, int E,
-                                bool no_dedup, GroupTable tab, int *scr, uint32_t *err_word) {
+                                bool no_dedup, GroupTable tab, int *scr, uint32_t *err_word,
+                                int tid0, int nthr, int bar) {
     const int C = T * (K + 1), n = T * K, K1 = K + 1;
-    const int tid = threadIdx.x, nthr = blockDim.x;
+    const int tid = (int)threadIdx.x - tid0;
     const int lane = tid & 31, warp = tid >> 5;
     int *e_first = scr, *e_group = scr + E, *e_count = scr + 2 * E;
-    int *sid = scr + 3 * E;  // the picks, read from global memory once
+    int *sid = group_table_picks(scr, E);  // the picks, read from global memory once
     int32_t *gexp = tab.gexp(), *gn = tab.gncols(), *g0 = tab.gcol0(), *crow = tab.col_row(),
             *rcol = tab.row_col();
 
@@ -72,8 +84,9 @@ __device__ void group_table_cta(const int32_t *__restrict__ ids, int T, int K, i
         e_first[e] = INT_MAX;
         e_count[e] = 0;
     }
-    for (int j = tid; j < n; j += nthr) sid[j] = ids[j];
-    __syncthreads();
+    if (ids)
+        for (int j = tid; j < n; j += nthr) sid[j] = ids[j];
+    gt_sync(bar, nthr);
 
     uint32_t err = 0;
     for (int j = tid; j < n; j += nthr) {
@@ -87,7 +100,7 @@ __device__ void group_table_cta(const int32_t *__restrict__ ids, int T, int K, i
             if (sid[t * K + q] == id) err |= kErrDupExpert;
     }
     if (err && err_word) atomicOr(err_word, err);
-    __syncthreads();
+    gt_sync(bar, nthr);
 
     if (warp == 0) {
         const unsigned lt = (1u << lane) - 1u;
@@ -180,7 +193,7 @@ __device__ void group_table_cta(const int32_t *__restrict__ ids, int T, int K, i
             tab.U() = 0;
         }
     }
-    __syncthreads();
+    gt_sync(bar, nthr);
 
     if (!no_dedup && T > 0) {
         for (int t = tid; t < T; t += nthr) {
@@ -195,7 +208,7 @@ __device__ void group_table_cta(const int32_t *__restrict__ ids, int T, int K, i
             crow[c] = t;
         }
     }
-    __syncthreads();
+    gt_sync(bar, nthr);
 }
 
 }  // namespace moe

@@ -49,7 +49,8 @@ struct WsHeader {
     uint32_t start_cnt;    // tensor-core path: CTA starts modulo 2*grid; start_cnt / grid = launch parity
     uint32_t job_next[2];  // tensor-core path, per parity: jobs claimed past the first round
     uint32_t x_ready[2];   // tensor-core path, per parity: CTAs done converting their activation slice
-    uint32_t pad[56];
+    uint32_t route_ready[2];  // tensor-core path, per parity: CTAs done with their router partial logits
+    uint32_t pad[54];
 };
 static_assert(sizeof(WsHeader) == 256, "header size");
 
