@@ -11,10 +11,14 @@ routed I=2048 NVFP4 E=256 top-8, shared I=2048 FP8 128x128 blocks, uniform
 routing). Four copies of the layer's weights are resident and the steps
 rotate over them, so each step reads weights that are not in L2 (126 MB).
 Every timing is also taken with the launches captured in a CUDA graph and
-replayed (`graph_us_per_launch`). The T=8 and T=64 workloads are timed too, under `sweep`
+replayed (`graph_us_per_launch`), and in `chain` the same launches back to back
+in four forms, alternating within every round: plain, chained (MOE_FLAG_CHAIN:
+each may start under the previous one), with the next layer's first
+shared-expert stages brought into L2 during each launch's tail
+(moe_fused_decode_next), and both. The T=8 and T=64 workloads are timed too, under `sweep`
 (--no-sweep skips them); --sweep-wide adds the wide-expert layer (E=384 top-8, uniform routing) at
 T = 1, 2, 4, ..., 256 with 4 distinct layers' weights resident, run back to
-back. --impl reference times the fp64 CPU oracle on whole launches of the
+back, plain and chained. --impl reference times the fp64 CPU oracle on whole launches of the
 same workload (the reference arm). Under torchrun every rank runs its own replica
 (the build has no cross-GPU exchange); rank 0 prints the max over ranks.
 """
@@ -48,7 +52,8 @@ KERNEL_SOURCES = ["moe_layer_decode_persistent_b300/csrc/api.cu",
                   "moe_layer_decode_persistent_b300/csrc/fused_tc.cuh",
                   "moe_layer_decode_persistent_b300/csrc/sm100.cuh",
                   "moe_layer_decode_persistent_b300/csrc/group_table.cuh",
-                  "moe_layer_decode_persistent_b300/csrc/moe_common.cuh"]
+                  "moe_layer_decode_persistent_b300/csrc/moe_common.cuh",
+                  "moe_layer_decode_persistent_b300/csrc/router.cuh"]
 
 
 def _code_only(text: str) -> str:
@@ -263,7 +268,7 @@ def run_ours(args, rank, world, local):
         clk.__exit__()
         return dict(us_launch=us_launch_max, ms_per_step=ms_per_step, algo_bytes=algo_bytes,
                     distinct=distinct, clocks=clk.summary(), err=err, e2e_us=None, h2d=0, d2h=0,
-                    sweep={}, wide={}, graph_us=None, T=shape.T, per_launch=per_launch)
+                    sweep={}, wide={}, graph_us=None, T=shape.T, per_launch=per_launch, chain=None)
     xh = L.x.cpu().pin_memory()
     ih = L.topk_ids.cpu().pin_memory()
     wh = L.topk_w.cpu().pin_memory()
@@ -290,6 +295,28 @@ def run_ours(args, rank, world, local):
     graph_us = graph_us_per_launch(launch_s, 4 * len(weights))
     assert B.moe_read_error(ws) == 0
 
+    # the same layers back to back in three more forms, alternating with the
+    # plain launches: chained (MOE_FLAG_CHAIN: each launch may start under the
+    # previous one), with the next layer's first shared-expert stages brought
+    # into L2 during each launch's tail (moe_fused_decode_next), and both
+    sh_c = B.make_shape(shape.T, shape.H, shape.I, shape.I_shared, shape.E, shape.K, args.flags | B.MOE_FLAG_CHAIN)
+
+    def launch_c(i, s):
+        rw, sw = weights[i % len(weights)]
+        B.moe_fused_decode(L.x, L.topk_ids, L.topk_w, rw, sw, out, sh_c, ws, stream=s)
+
+    def launch_n(i, s, sh_=sh):
+        rw, sw = weights[i % len(weights)]
+        nsw = weights[(i + 1) % len(weights)][1]
+        B.moe_fused_decode_next(L.x, L.topk_ids, L.topk_w, rw, sw, nsw, out, sh_, ws, stream=s)
+
+    def launch_nc(i, s):
+        launch_n(i, s, sh_c)
+
+    chain = None if args.no_chain else chain_ab(
+        {"plain": launch_s, "chain": launch_c, "next": launch_n, "next_chain": launch_nc}, 4 * len(weights))
+    assert B.moe_read_error(ws) == 0
+
     # the other workloads of the metric (T=8, T=64) and the routed T=1 layer,
     # unless --no-sweep
     del copies, weights
@@ -307,7 +334,7 @@ def run_ours(args, rank, world, local):
     return dict(us_launch=us_launch_max, ms_per_step=ms_per_step, algo_bytes=algo_bytes,
                 distinct=distinct, clocks=clk.summary(), err=err, e2e_us=e2e_us,
                 h2d=xh.numel() * 2 + ih.numel() * 4 + wh.numel() * 4, d2h=oh.numel() * 2,
-                sweep=sweep, wide=wide, graph_us=graph_us, T=shape.T, per_launch=per_launch)
+                sweep=sweep, wide=wide, graph_us=graph_us, T=shape.T, per_launch=per_launch, chain=chain)
 
 
 def graph_us_per_launch(launch, n_launch: int, reps: int = 5) -> float:
@@ -335,6 +362,71 @@ def graph_us_per_launch(launch, n_launch: int, reps: int = 5) -> float:
         b.record(s)
     torch.cuda.synchronize()
     return a.elapsed_time(b) * 1e3 / (reps * n_launch)
+
+
+def capture_graph(launch, n_launch: int):
+    """n_launch launches captured in one CUDA graph on a side stream."""
+    import torch
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        launch(0, s)  # warm (outside capture)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            for i in range(n_launch):
+                launch(i, s)
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    return g, s
+
+
+def chain_ab(variants: dict, n_launch: int, rounds: int = 3, reps: int = 3) -> dict:
+    """Layers back to back in several forms (name -> launch(i, stream)), all
+    forms alternating within every round: eagerly (n_launch launches between
+    two events) and as CUDA-graph replays. Medians over the rounds, us per
+    launch: `<name>_us_per_launch` and `<name>_graph_us_per_launch`."""
+    import torch
+    st = torch.cuda.current_stream()
+
+    def eager(f):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        for i in range(n_launch):
+            f(i, st)
+        b.record(st)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) * 1e3 / n_launch
+
+    def replay(gs):
+        g, s = gs
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            a.record(s)
+            for _ in range(reps):
+                g.replay()
+            b.record(s)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) * 1e3 / (reps * n_launch)
+
+    for f in variants.values():
+        for i in range(n_launch):
+            f(i, st)
+    torch.cuda.synchronize()
+    graphs = {k: capture_graph(f, n_launch) for k, f in variants.items()}
+    t = {}
+    for _ in range(rounds):
+        for k, f in variants.items():
+            t.setdefault(f"{k}_us_per_launch", []).append(eager(f))
+            t.setdefault(f"{k}_graph_us_per_launch", []).append(replay(graphs[k]))
+    del graphs
+    out = {k: round(statistics.median(v), 2) for k, v in t.items()}
+    out["layers_back_to_back"] = n_launch
+    out["rounds"] = rounds
+    return out
 
 
 def sweep_point(name, args, dev):
@@ -492,13 +584,26 @@ def wide_sweep(args, dev, n_layers: int = 4):
         torch.cuda.synchronize()
         us = a.elapsed_time(b) * 1e3 / n
         g_us = graph_us_per_launch(launch_s, 2 * n_layers)
+        sh_c = B.make_shape(T, shape.H, shape.I, shape.I_shared, E, shape.K, args.flags | B.MOE_FLAG_CHAIN)
+
+        def launch_c(i, s, sh_c=sh_c, ws=ws, out=out, x=x, ids=ids, w=w):
+            _, _, rw, sw = layers[i % n_layers]
+            B.moe_fused_decode(x, ids, w, rw, sw, out, sh_c, ws, stream=s)
+
+        def launch_n(i, s, sh_=sh, ws=ws, out=out, x=x, ids=ids, w=w):
+            _, _, rw, sw = layers[i % n_layers]
+            nsw = layers[(i + 1) % n_layers][3]
+            B.moe_fused_decode_next(x, ids, w, rw, sw, nsw, out, sh_, ws, stream=s)
+
+        chain = chain_ab({"plain": launch_s, "chain": launch_c, "next": launch_n,
+                          "next_chain": lambda i, s_, sh_c=sh_c, f=launch_n: f(i, s_, sh_c)}, 2 * n_layers)
         assert B.moe_read_error(ws) == 0
         distinct = len(set(int(e) for e in ids.cpu().reshape(-1).tolist()))
         byt = distinct * layers[0][0].nbytes_expert() + layers[0][1].nbytes_expert() + 4 * T * shape.H + 8 * T * shape.K
         gbs = byt / (us * 1e-6) / 1e9
         res[str(T)] = {"us_per_launch": round(us, 2), "graph_us_per_launch": round(g_us, 2),
                        "hbm_gbs": round(gbs, 1), "frac": round(gbs / peak, 4), "distinct_experts": distinct,
-                       "algo_bytes": byt}
+                       "algo_bytes": byt, "chain_ab": chain}
         del ws, out
     del layers
     torch.cuda.empty_cache()
@@ -597,6 +702,8 @@ def main():
                     help="skip the T=8 and T=64 workloads (timed by default, under `sweep`)")
     ap.add_argument("--sweep-wide", action="store_true",
                     help="also time the wide-expert layer (E=384) at T=1..256, 4 layers back to back")
+    ap.add_argument("--no-chain", action="store_true",
+                    help="skip the back-to-back forms (chained, next-layer prefetch) of the main workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer (end-to-end) timing")
     ap.add_argument("--experts", type=int, default=256,
@@ -655,6 +762,8 @@ def main():
         "gpu_launches": args.steps, "clocks": r["clocks"], "device_error_word": r["err"],
         "graph_us_per_launch": None if r["graph_us"] is None else round(r["graph_us"], 2),
     }
+    if r["chain"]:
+        line["chain"] = r["chain"]
     if r["sweep"]:
         line["sweep"] = r["sweep"]
     if r["wide"]:

@@ -65,9 +65,20 @@ enum {
                                  row's shared use is its own 1-column group */
     MOE_FLAG_FORCE_FMA = 2u,  /* CUDA-core dequant-GEMV contraction */
     MOE_FLAG_FORCE_MMA = 4u,  /* tcgen05 tensor-core contraction */
-    MOE_FLAG_DEBUG_DROP_ARRIVE = 8u /* fault injection: one CTA skips one
+    MOE_FLAG_DEBUG_DROP_ARRIVE = 8u, /* fault injection: one CTA skips one
                                  inter-CTA arrival, so the waits on it time out
                                  and set MOE_DEV_WAIT_TIMEOUT */
+    MOE_FLAG_CHAIN = 16u      /* layers back to back: the launch may start
+                                 while the previous kernel on the stream still
+                                 runs (programmatic dependent launch). Each CTA
+                                 sets up its barriers and tensor memory and
+                                 streams its first shared-expert weights, then
+                                 waits for the previous grid to complete before
+                                 it reads any input or the workspace, so the
+                                 result is the same bits as without the flag
+                                 and the previous kernel may produce this
+                                 launch's inputs. Only weights must not be
+                                 written by the previous kernel. */
 };
 
 /* Weight storage formats. */
@@ -175,6 +186,29 @@ moe_status moe_fused_decode(const void *x, const int32_t *topk_ids,
                             const moe_weights *shared, void *out,
                             const moe_shape *s, void *workspace,
                             size_t workspace_bytes, void *stream);
+
+/*
+ * moe_fused_decode for layers run back to back: the same computation and
+ * arguments, plus next_shared, the shared expert of the layer launched next
+ * with the same shape (same format, H and I_shared; device memory, not
+ * written before that launch). Once this launch has handed out its last job,
+ * each CTA requests into L2 the first weight stages of the next layer's
+ * shared expert that the same CTA of that launch loads before its group
+ * table, so those arrive from L2 while the next launch builds its table
+ * ("Daily AI Hotspot 2026-08-21", "Most Worth Your Attention Today": the
+ * persistent kernel's start-up cost; PR #27 "each expert once",
+ * "Modifications": weight loads issued ahead of every wait). A prefetch moves
+ * no result: the output is the same bits as moe_fused_decode's. The
+ * CUDA-core contraction ignores the hint. Errors: those of moe_fused_decode,
+ * and MOE_ERR_INVALID_ARG when next_shared is NULL, incomplete, misaligned or
+ * of another format than `shared`.
+ */
+moe_status moe_fused_decode_next(const void *x, const int32_t *topk_ids,
+                                 const float *topk_w, const moe_weights *routed,
+                                 const moe_weights *shared,
+                                 const moe_weights *next_shared, void *out,
+                                 const moe_shape *s, void *workspace,
+                                 size_t workspace_bytes, void *stream);
 
 /*
  * The same layer called with HOST buffers for the step's inputs and output

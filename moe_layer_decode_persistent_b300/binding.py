@@ -15,12 +15,13 @@ LIB_PATH = os.path.join(PKG, "libmoe.so")
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA = range(5)
 MOE_DEV_BAD_EXPERT, MOE_DEV_DUP_EXPERT, MOE_DEV_WAIT_TIMEOUT, MOE_DEV_RANGE = 1, 2, 4, 8
-MOE_FLAG_NO_DEDUP, MOE_FLAG_FORCE_FMA, MOE_FLAG_FORCE_MMA, MOE_FLAG_DEBUG_DROP_ARRIVE = 1, 2, 4, 8
+MOE_FLAG_NO_DEDUP, MOE_FLAG_FORCE_FMA, MOE_FLAG_FORCE_MMA, MOE_FLAG_DEBUG_DROP_ARRIVE, MOE_FLAG_CHAIN = 1, 2, 4, 8, 16
 MOE_W_BF16, MOE_W_NVFP4, MOE_W_FP8_B128 = 0, 1, 2
 
 # every symbol include/moe.h declares
 EXPORTS = ("moe_workspace_bytes", "moe_workspace_bytes_host", "moe_workspace_init",
-           "moe_group_table_ints", "moe_group_table", "moe_fused_decode", "moe_fused_decode_host",
+           "moe_group_table_ints", "moe_group_table", "moe_fused_decode", "moe_fused_decode_next",
+           "moe_fused_decode_host",
            "moe_fused_decode_noalloc", "moe_route", "moe_fused_decode_routed", "moe_read_error",
            "moe_status_string", "moe_last_error_detail")
 
@@ -73,6 +74,8 @@ def lib():
         L.moe_group_table.argtypes = [P, sp, P, P, S, P]
         L.moe_fused_decode.restype = I
         L.moe_fused_decode.argtypes = [P, P, P, wp, wp, P, sp, P, S, P]
+        L.moe_fused_decode_next.restype = I
+        L.moe_fused_decode_next.argtypes = [P, P, P, wp, wp, wp, P, sp, P, S, P]
         L.moe_fused_decode_host.restype = I
         L.moe_fused_decode_host.argtypes = [P, P, P, wp, wp, P, sp, P, S, P]
         L.moe_fused_decode_noalloc.restype = I
@@ -157,6 +160,17 @@ def moe_fused_decode(x, topk_ids, topk_w, routed: moe_weights, shared: moe_weigh
     st = lib().moe_fused_decode(_ptr(x), _ptr(topk_ids), _ptr(topk_w), ctypes.byref(routed),
                                 ctypes.byref(shared), _ptr(out), ctypes.byref(shape), _ptr(ws), n,
                                 _stream(stream))
+    return _check(st) if check else st
+
+
+def moe_fused_decode_next(x, topk_ids, topk_w, routed: moe_weights, shared: moe_weights,
+                          next_shared: moe_weights, out, shape: moe_shape, ws, stream=None, check=True):
+    """moe_fused_decode that also brings the next layer's first shared-expert
+    stages into L2 during its tail (same result bits)."""
+    st = lib().moe_fused_decode_next(_ptr(x), _ptr(topk_ids), _ptr(topk_w), ctypes.byref(routed),
+                                     ctypes.byref(shared), ctypes.byref(next_shared), _ptr(out),
+                                     ctypes.byref(shape), _ptr(ws), ws.numel() * ws.element_size(),
+                                     _stream(stream))
     return _check(st) if check else st
 
 

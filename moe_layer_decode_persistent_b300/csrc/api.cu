@@ -59,7 +59,7 @@ struct WsLayout {
     size_t route = 0;  // router partial logits [T][E][kRouterParts] fp32 (routed launches)
     size_t mid = 0, y = 0, fma_end = 0;
     size_t tc_ready = 0, tc_htile = 0, tc_tile = 0, tc_ctrl_end = 0, tc_P = 0, tc_Y = 0, tc_midB = 0,
-           tc_xh = 0, tc_end = 0;
+           tc_xh = 0, tc_xs = 0, tc_end = 0;
     size_t dev_total = 0;
     size_t st_x = 0, st_ids = 0, st_w = 0, st_out = 0, host_total = 0;
 };
@@ -108,6 +108,8 @@ WsLayout ws_layout(const moe_shape *s) {
     off += cols_padded * (Imax / 128) * 256;
     L.tc_xh = off = align_up(off, 256);
     off += T * H * 2;
+    L.tc_xs = off = align_up(off, 256);
+    off += T * 4;
     L.tc_end = align_up(off, 256);
 
     L.route = off = std::max(L.fma_end, L.tc_end);
@@ -142,7 +144,7 @@ moe_status check_shape(const moe_shape *s) {
             return fail(MOE_ERR_UNSUPPORTED, "%s=%d is not a multiple of 128", names[i], dims[i]);
     }
     const unsigned known = MOE_FLAG_NO_DEDUP | MOE_FLAG_FORCE_FMA | MOE_FLAG_FORCE_MMA |
-                           MOE_FLAG_DEBUG_DROP_ARRIVE;
+                           MOE_FLAG_DEBUG_DROP_ARRIVE | MOE_FLAG_CHAIN;
     if (s->flags & ~known) return fail(MOE_ERR_INVALID_ARG, "unknown flag bits 0x%x", s->flags & ~known);
     if ((s->flags & MOE_FLAG_FORCE_FMA) && (s->flags & MOE_FLAG_FORCE_MMA))
         return fail(MOE_ERR_INVALID_ARG, "FORCE_FMA and FORCE_MMA both set");
@@ -282,6 +284,41 @@ moe_status plan_occupancy(Kern k, int dev, int threads, size_t smem, const DevIn
     return MOE_OK;
 }
 
+// Launches a fused kernel cooperatively: every CTA resident at once, or the
+// launch fails. A chained launch (MOE_FLAG_CHAIN) also carries programmatic
+// stream serialization, so it may start while the previous kernel on the
+// stream still runs. Where the runtime refuses the two attributes together,
+// chained launches on that device go without the cooperative one: the grid is
+// still one wave by the occupancy calculation, and every inter-CTA wait is
+// bounded, so a grid that could not be all resident ends with
+// MOE_DEV_WAIT_TIMEOUT instead of hanging.
+std::atomic<int> g_chain_coop[kMaxDevices];  // 0 untried, 1 accepted, 2 refused
+
+template <typename P>
+moe_status launch_persistent(cudaLaunchConfig_t cfg, void (*kern)(P), const P &p, bool chain, int dev,
+                             const char *what) {
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    const bool both = chain && g_chain_coop[dev].load(std::memory_order_relaxed) != 2;
+    cfg.attrs = (chain && !both) ? attr + 1 : attr;
+    cfg.numAttrs = both ? 2 : 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
+    if (both && (e == cudaErrorInvalidValue || e == cudaErrorNotSupported)) {
+        (void)cudaGetLastError();  // a refused configuration, not a device error
+        g_chain_coop[dev].store(2);
+        cfg.attrs = attr + 1;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, kern, p);
+    } else if (both && e == cudaSuccess) {
+        g_chain_coop[dev].store(1, std::memory_order_relaxed);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, what);
+    return MOE_OK;
+}
+
 moe_status launch_fused_fma(const moe::FusedParams &p, const moe_shape *s, int dev, const DevInfo &d,
                             cudaStream_t stream) {
     const size_t smem = table_smem_bytes(s);
@@ -293,14 +330,8 @@ moe_status launch_fused_fma(const moe::FusedParams &p, const moe_shape *s, int d
     cfg.blockDim = dim3(moe::kFmaThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, moe::fused_fma_kernel, p);
-    if (e != cudaSuccess) return cuda_fail(e, "launch fused_fma_kernel");
-    return MOE_OK;
+    return launch_persistent(cfg, moe::fused_fma_kernel, p, (s->flags & MOE_FLAG_CHAIN) != 0, dev,
+                             "launch fused_fma_kernel");
 }
 
 // ---- tensor maps (cached: encoding costs microseconds of host time) ----------
@@ -441,8 +472,8 @@ bool tc_eligible(const moe_shape *s, const moe_weights *routed, const moe_weight
 }
 
 moe_status launch_fused_tc(const moe::FusedParams &fp, const WsLayout &L, const moe_shape *s,
-                           const moe_weights *routed, const moe_weights *shared, int dev, const DevInfo &d,
-                           cudaStream_t stream) {
+                           const moe_weights *routed, const moe_weights *shared, const moe_weights *next_shared,
+                           int dev, const DevInfo &d, cudaStream_t stream) {
     moe::TcParams p;
     memset(&p, 0, sizeof p);
     moe_status st = tc_maps(routed, shared, s, &p.maps);
@@ -460,6 +491,10 @@ moe_status launch_fused_tc(const moe::FusedParams &fp, const WsLayout &L, const 
     p.E = s->E;
     p.K = s->K;
     p.flags = s->flags;
+    if (next_shared) {
+        p.nx13 = static_cast<const uint8_t *>(next_shared->w13);
+        p.nx13s = static_cast<const uint8_t *>(next_shared->w13_scale);
+    }
     char *ws = reinterpret_cast<char *>(fp.hdr);
     p.hdr = fp.hdr;
     p.group_ready = reinterpret_cast<uint32_t *>(ws + L.tc_ready);
@@ -469,6 +504,7 @@ moe_status launch_fused_tc(const moe::FusedParams &fp, const WsLayout &L, const 
     p.Y = reinterpret_cast<float *>(ws + L.tc_Y);
     p.midB = reinterpret_cast<uint8_t *>(ws + L.tc_midB);
     p.xh = reinterpret_cast<__half *>(ws + L.tc_xh);
+    p.xs = reinterpret_cast<int32_t *>(ws + L.tc_xs);
     p.Ucap = s->T * (s->K + 1);
     p.Imax = std::max(s->I, s->I_shared);
     p.route_mode = fp.route_mode;
@@ -502,14 +538,7 @@ moe_status launch_fused_tc(const moe::FusedParams &fp, const WsLayout &L, const 
     cfg.blockDim = dim3(moe::kTcThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
-    if (e != cudaSuccess) return cuda_fail(e, "launch fused_tc_kernel");
-    return MOE_OK;
+    return launch_persistent(cfg, kern, p, (s->flags & MOE_FLAG_CHAIN) != 0, dev, "launch fused_tc_kernel");
 }
 
 // CUDA-core scratch laid out straight after the header (no tensor-path
@@ -553,11 +582,18 @@ moe_status fused_decode_impl(const void *x, const int32_t *ids, const float *w,
                              const moe_weights *routed, const moe_weights *shared, void *out,
                              const moe_shape *s, void *ws, size_t ws_bytes, cudaStream_t stream,
                              bool fma_compact = false, const moe_router *router = nullptr,
-                             int32_t *ids_out = nullptr, float *w_out = nullptr) {
+                             int32_t *ids_out = nullptr, float *w_out = nullptr,
+                             const moe_weights *next_shared = nullptr) {
     moe_status st = check_shape(s);
     if (st != MOE_OK) return st;
     if ((st = check_weights(routed, "routed")) != MOE_OK) return st;
     if ((st = check_weights(shared, "shared")) != MOE_OK) return st;
+    if (next_shared) {
+        if ((st = check_weights(next_shared, "next shared")) != MOE_OK) return st;
+        if (next_shared->fmt != shared->fmt)
+            return fail(MOE_ERR_INVALID_ARG, "next shared weights: format %d, this layer's is %d", next_shared->fmt,
+                        shared->fmt);
+    }
     if (router && (st = check_router(router, s)) != MOE_OK) return st;
     if (!ws) return fail(MOE_ERR_INVALID_ARG, "workspace is NULL");
     if (!aligned(ws, 256)) return fail(MOE_ERR_INVALID_ARG, "workspace not 256-byte aligned");
@@ -616,7 +652,7 @@ moe_status fused_decode_impl(const void *x, const int32_t *ids, const float *w,
     p.route_mode = router ? 1 : 0;
     memset(&p.router, 0, sizeof p.router);
     if (router) p.router = router_dev(router, L, ws, ids_out, w_out);
-    if (use_tc) return launch_fused_tc(p, L, s, routed, shared, dev, d, stream);
+    if (use_tc) return launch_fused_tc(p, L, s, routed, shared, next_shared, dev, d, stream);
     return launch_fused_fma(p, s, dev, d, stream);
 }
 
@@ -757,6 +793,15 @@ moe_status moe_fused_decode(const void *x, const int32_t *topk_ids, const float 
                             void *stream) {
     return fused_decode_impl(x, topk_ids, topk_w, routed, shared, out, s, workspace,
                              workspace_bytes, (cudaStream_t)stream);
+}
+
+moe_status moe_fused_decode_next(const void *x, const int32_t *topk_ids, const float *topk_w,
+                                 const moe_weights *routed, const moe_weights *shared,
+                                 const moe_weights *next_shared, void *out, const moe_shape *s, void *workspace,
+                                 size_t workspace_bytes, void *stream) {
+    if (!next_shared) return fail(MOE_ERR_INVALID_ARG, "next shared weights struct is NULL");
+    return fused_decode_impl(x, topk_ids, topk_w, routed, shared, out, s, workspace, workspace_bytes,
+                             (cudaStream_t)stream, false, nullptr, nullptr, nullptr, next_shared);
 }
 
 moe_status moe_route(const void *x, const moe_router *router, int32_t *topk_ids, float *topk_w,

@@ -25,6 +25,7 @@
 #include "group_table.cuh"
 #include "moe_common.cuh"
 #include "router.cuh"
+#include "sm100.cuh"
 
 namespace moe {
 
@@ -218,6 +219,7 @@ __global__ void __launch_bounds__(kFmaThreads) fused_fma_kernel(FusedParams p) {
     const int nwarps_cta = blockDim.x >> 5;
     const int gw = blockIdx.x * nwarps_cta + (threadIdx.x >> 5);
     const int nw = gridDim.x * nwarps_cta;
+    sm100::griddep_wait();  // a chained launch: the previous grid's writes first
 
     // ---- phase R (routed launches): partial logits over every warp of the
     // grid, then each CTA picks every row's experts on chip ----------------
@@ -230,6 +232,7 @@ __global__ void __launch_bounds__(kFmaThreads) fused_fma_kernel(FusedParams p) {
     group_table_cta(p.route_mode ? nullptr : p.ids, T, K, p.E, no_dedup, tab, scr,
                     blockIdx.x == 0 ? &p.hdr->err : nullptr, 0, blockDim.x, 0);
     const float *topk_w = p.route_mode ? tw_s : p.topk_w;
+    sm100::griddep_launch_dependents();
 
     const int G = tab.G();
     const int32_t *gexp = tab.gexp(), *gn = tab.gncols(), *g0 = tab.gcol0(),

@@ -136,11 +136,14 @@ struct TcParams {
     float *P;               // gate/up partials [kc][2][Ucap][Imax]
     float *Y;               // down partials [kc][Ucap][H]
     uint8_t *midB;          // f16 intermediate in MMA B layout
-    __half *xh;             // the activations as f16 [T][H]
+    __half *xh;             // the activations as f16 [T][H], each row scaled by 2^-xs[t]
+    int32_t *xs;            // [T] the rows' activation scale exponents (0 <= xs <= 63)
     int Ucap, Imax;
     int route_mode;         // 1: the picks and weights come from the router, not ids/topk_w
     RouterDev router;
     TcFmt fc[2];            // 0: shared expert, 1: routed experts
+    const uint8_t *nx13;    // or null: the next layer's shared gate/up weights (same shape and format),
+    const uint8_t *nx13s;   // and their NVFP4 block scales; their first stages are requested into L2
 };
 
 struct TcJob {
@@ -190,17 +193,19 @@ struct TcSmem {
     static constexpr int bbuf = 0;
     static constexpr int jobs = bbuf + kASlotsMax * kBUnitBytes;
     static constexpr int bars = jobs + kJobSlots * (int)sizeof(TcJob);
-    // jfull, jempty, rfull, rempty, sfull, sempty, dfull, dempty, drain[4], coef
-    static constexpr int nbars = 2 * kJobSlots + 2 * kRawStagesMax + 2 * kASlotsMax + 2 * 2 + kIssuers + 1;
+    // jfull, jempty, rfull, rempty, sfull, sempty, dfull, dempty, drain[4], coef, xs
+    static constexpr int nbars = 2 * kJobSlots + 2 * kRawStagesMax + 2 * kASlotsMax + 2 * 2 + kIssuers + 2;
     static constexpr int misc = bars + nbars * 8;  // tmem addr, abort, down jobs per tile, parity
     static constexpr int tile_ready = misc + 64;   // per 256-row output tile: combine may start (64 max)
-    static constexpr int tables = tile_ready + 256;  // group table, then per-group arrays
+    static constexpr int red = tile_ready + 256;     // row-maximum reduction scratch (32 ints)
+    static constexpr int tables = red + 128;         // group table, then per-group arrays
 };
 constexpr int kTcGroupArrays = 5;  // gu, dn, tile, mid and pair prefix sums
 
 // The group table (per-group arrays of capacity gcap), the per-group prefix
 // sums (gcap + 1 each), then two float arrays of C = T*(K+1): each (row, slot)'s
-// combine weight and down global scale (slot 0 = shared expert). Up to
+// combine weight and down global scale (slot 0 = shared expert), then the T
+// rows' activation scale exponents. Up to
 // kTcFullTablesMaxT rows the per-group arrays hold C entries (the compiler then
 // sees a fixed layout); above, they hold the group capacity so the tables fit.
 constexpr int kTcFullTablesMaxT = 64;
@@ -210,7 +215,7 @@ __host__ __device__ inline int tc_gcap(int T, int K, int E, bool no_dedup) {
 }
 __host__ __device__ inline int tc_raw_offset(int T, int K, int gcap) {
     const int C = T * (K + 1);
-    const int end = TcSmem::tables + 4 * (group_table_ints_cap(T, K, gcap) + kTcGroupArrays * (gcap + 1) + 2 * C);
+    const int end = TcSmem::tables + 4 * (group_table_ints_cap(T, K, gcap) + kTcGroupArrays * (gcap + 1) + 2 * C + T + 1);
     return (end + 1023) & ~1023;
 }
 // Dynamic shared memory for nR raw stages (+1024 to align the base).
@@ -232,39 +237,116 @@ __device__ __forceinline__ int group_of_col(const int32_t *g0, int G, int c) {
     return lo;
 }
 
-// The activations -> f16 [T][H], the gate/up MMA's B operand (bf16 -> f16 is
-// exact for |x| in [2^-17, 65504]; larger magnitudes set MOE_DEV_RANGE). The
-// 16-byte items are dealt over `nthr` threads of the grid (this one is `gt`),
-// four loads in flight per thread.
-__device__ __forceinline__ void tc_convert_x(const TcParams &p, int gt, int nthr) {
-    const int n = p.T * p.H / 8;
-    const uint4 *src = reinterpret_cast<const uint4 *>(p.x);
+// The activations -> f16 [T][H], the gate/up MMA's B operand, each row t
+// scaled by an exact power of two 2^-s_t: s_t = 0 while the row's largest
+// magnitude is below 16, else the shift that brings it into [8, 16) (at most
+// 63). Rows without a shift convert exactly as bf16 -> f16 (exact for |x| in
+// [2^-17, 65504]); a shifted row keeps f16's 11 bits for everything within
+// 2^-24 of its largest element. The gate/up epilogue undoes the shift inside
+// the SwiGLU and the combine undoes its square, so results are unchanged
+// except where f16 would have overflowed (MOE_DEV_RANGE now only for
+// non-finite inputs or intermediates).
+//
+// Rows are shared out over the CTAs: with T < grid, the CTAs b = t + T*k
+// (k < grid / T) split row t's 16-byte items between them; with T >= grid,
+// CTA b converts rows b, b + grid, ... whole. Each CTA finds the maximum of
+// the rows it touches itself (a reduction over warps 1.. behind named barrier
+// `bar`), so the shift needs no exchange between CTAs; the CTA holding a
+// row's first slice writes s_t.
+constexpr int kMaxActShift = 63;
+// The raw stages that CTA b requests before its group table is built: its
+// first job, when that is one of the shared expert's gate/up jobs (the shared
+// expert is group 0 in either form and its gate/up jobs come first in the
+// list), which the launch's shape alone defines. Returns how many stages (0:
+// the first job is another one), with the job's 128-row tile and first K
+// element.
+__device__ __forceinline__ int tc_first_stages(const TcParams &p, bool no_dedup, int nR, int *tile, int *k0) {
+    const TcFmt &f0 = p.fc[0];
+    const int n0 = no_dedup ? 1 : p.T;
+    const int tiles0 = f0.tiles, nkc0 = f0.nkc_gu, b = (int)blockIdx.x;
+    if (b >= ((n0 + f0.nt - 1) >> f0.nt_shift) * tiles0 * nkc0) return 0;
+    const int rem = b % (tiles0 * nkc0), kc = rem % nkc0;
+    *tile = rem / nkc0;
+    *k0 = kc * f0.kc_gu;
+    const bool fp4 = p.shared.fmt == kFmtNvfp4;
+    const int nst = (min(f0.kc_gu, p.H - *k0) / kUnitK) / (fp4 ? 2 : 1);
+    return min(nst, nR - 1);
+}
+
+__device__ __forceinline__ int act_shift(uint32_t max_abs_bits) {
+    const int e = (int)(max_abs_bits >> 7) - 127;  // bf16 exponent of the largest magnitude
+    return (max_abs_bits >= 0x7f80u) ? 0 : max(0, min(e - 3, kMaxActShift));
+}
+
+__device__ __forceinline__ bool tc_convert_rows(const TcParams &p, int tid1, int nthr1, int bar, uint32_t *red_s) {
+    constexpr int kMaxItems = 4;  // 16-byte items of a row a thread holds: H <= 16384, 17 warps
+    const int T = p.T, G = (int)gridDim.x, b = (int)blockIdx.x;
+    const int n8 = p.H / 8;  // 16-byte items per row
+    const int nsl = T < G ? G / T : 1;  // CTAs per row
+    const int t0 = T < G ? b % T : b, dt = T < G ? T : G;
+    const int sl = T < G ? b / T : 0;
+    bool shifted = false;  // some row of this CTA's share is shifted (meaningful on tid1 0)
+    if (sl >= nsl) return shifted;  // no slice for this CTA
     uint4 *dst = reinterpret_cast<uint4 *>(p.xh);
     uint32_t range_bad = 0;
-    for (int i0 = gt; i0 < n; i0 += 4 * nthr) {
-        uint4 v[4];
+    for (int t = t0; t < T; t += dt) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(p.x) + (size_t)t * n8;
+        // the row's largest magnitude (bf16 bits without sign: monotone); the
+        // items stay in registers for the conversion below
+        uint4 v[kMaxItems];
+        uint32_t mx = 0;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int it = i0 + j * nthr;
-            v[j] = it < n ? __ldg(src + it) : make_uint4(0u, 0u, 0u, 0u);
+        for (int k = 0; k < kMaxItems; ++k) {
+            const int i = tid1 + k * nthr1;
+            v[k] = i < n8 ? __ldg(src + i) : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int it = i0 + j * nthr;
-            if (it >= n) break;
-            const uint32_t w4[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+        for (int k = 0; k < kMaxItems; ++k) {
+            const uint32_t w4[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) mx = max(mx, max(w4[q] & 0x7fffu, (w4[q] >> 16) & 0x7fffu));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if ((tid1 & 31) == 0) red_s[tid1 >> 5] = mx;
+        sm100::named_bar_sync(bar, nthr1);
+        uint32_t rowmax = 0;
+        for (int w = 0; w < nthr1 / 32; ++w) rowmax = max(rowmax, red_s[w]);
+        sm100::named_bar_sync(bar, nthr1);  // red_s may be reused for the next row
+        const int sh = act_shift(rowmax);
+        const float f = __uint_as_float((uint32_t)(127 - sh) << 23);  // 2^-sh, exact
+        if (sl == 0 && tid1 == 0) p.xs[t] = sh;
+        shifted |= sh != 0;
+        // this CTA's slice of the row's items
+        const int i0 = (int)((long long)n8 * sl / nsl), i1 = (int)((long long)n8 * (sl + 1) / nsl);
+#pragma unroll
+        for (int k = 0; k < kMaxItems; ++k) {
+            const int i = tid1 + k * nthr1;
+            if (i < i0 || i >= i1) continue;
+            const uint32_t w4[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
             uint32_t o[4];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const __half2 h = __floats2half2_rn(bf16_bits_to_float(w4[k] & 0xffffu), bf16_bits_to_float(w4[k] >> 16));
+            for (int q = 0; q < 4; ++q) {
+                const __half2 h = __floats2half2_rn(__fmul_rn(bf16_bits_to_float(w4[q] & 0xffffu), f),
+                                                    __fmul_rn(bf16_bits_to_float(w4[q] >> 16), f));
                 if (__hisinf(__low2half(h)) || __hisinf(__high2half(h))) range_bad = 1;
-                o[k] = pack_h2(h);
+                o[q] = pack_h2(h);
             }
-            dst[it] = make_uint4(o[0], o[1], o[2], o[3]);
+            dst[(size_t)t * n8 + i] = make_uint4(o[0], o[1], o[2], o[3]);
         }
     }
     if (range_bad) atomicOr(&p.hdr->err, kErrRange);
+    return shifted;
 }
+static_assert(16384 / 8 <= 4 * (kTcThreads - 32), "a row's items fit the converting threads' registers");
+
+// SwiGLU of a column whose activations were scaled by 2^-s (g, u: the scaled
+// gate and up sums, global scales applied; fs = 2^s, fis = 2^-s): the true
+// silu(g 2^s) (u 2^s), scaled by 2^-2s. With s = 0 it is silu(g) u exactly.
+__device__ __forceinline__ float swiglu_scaled(float g, float u, float fs, float fis) {
+    return __fmul_rn(__fmul_rn(silu_f32(__fmul_rn(g, fs)), fis), u);
+}
+__device__ __forceinline__ float pow2f(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }  // |e| <= 126
 
 // kRouted: the picks and weights come from the router inside the launch (a
 // separate instantiation, so the router's registers never weigh on the
@@ -293,6 +375,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
     uint64_t *dfull = sempty + kASlotsMax, *dempty = dfull + 2;
     uint64_t *drain = dempty + 2;
     uint64_t *coef_bar = drain + kIssuers;  // the combine coefficients are filled
+    uint64_t *xs_bar = coef_bar + 1;        // the rows' activation scales are in xs_s
     uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(smem + TcSmem::misc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + TcSmem::misc + 4);
     int *dn_per_ht_s = reinterpret_cast<int *>(smem + TcSmem::misc + 8);
@@ -307,6 +390,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
     int *pair_prefix = mid_prefix + (gcap + 1);
     float *comb_w = reinterpret_cast<float *>(pair_prefix + (gcap + 1));  // [T][K+1]
     float *comb_g = comb_w + C;                                        // [T][K+1]
+    int32_t *xs_s = reinterpret_cast<int32_t *>(comb_g + C);           // [T + 1]
     uint32_t *err = &p.hdr->err;
 
     // ---- prologue -----------------------------------------------------------
@@ -348,33 +432,35 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
         }
         for (int i = 0; i < kIssuers; ++i) mbar_init(&drain[i], 1);
         mbar_init(coef_bar, 4);  // one arrival per epilogue warp
+        mbar_init(xs_bar, 1);    // the first epilogue warp
         for (int i = 0; i < 64; ++i) tile_ready_s[i] = 0;
         *abort_flag = 0;
         fence_mbar_init();
-        // The shared expert is group 0 in either form and its gate/up jobs come
-        // first in the list, so when this CTA's first job (job b) is one of them
-        // the shape alone defines it: its first stages stream in while the group
-        // table is built (the table's scratch sits in the ring's last stage).
-        const TcFmt &f0 = p.fc[0];
-        const int fmt0 = p.shared.fmt, n0 = no_dedup ? 1 : T;
-        const int tiles0 = f0.tiles, nkc0 = f0.nkc_gu, b = (int)blockIdx.x;
-        if (b < ((n0 + f0.nt - 1) >> f0.nt_shift) * tiles0 * nkc0) {
+        // When this CTA's first job is one of the shared expert's gate/up jobs,
+        // its first stages stream in while the group table is built (the
+        // table's scratch sits in the ring's last stage). Weights only: they
+        // are constant, so a chained launch may request them at once.
+        int tile0 = 0, k00 = 0;
+        npre = tc_first_stages(p, no_dedup, nR, &tile0, &k00);
+        if (npre) {
             fence_proxy_async_smem();
-            const int rem = b % (tiles0 * nkc0), tile = rem / nkc0, kc = rem - tile * nkc0;
-            const int kc_len = f0.kc_gu, k0 = kc * kc_len;
-            const bool fp4 = fmt0 == kFmtNvfp4;
-            const int nst = (min(kc_len, H - k0) / kUnitK) / (fp4 ? 2 : 1);
-            npre = min(nst, nR - 1);
+            const bool fp4 = p.shared.fmt == kFmtNvfp4;
             const uint64_t pol = l2_evict_first_policy();
             for (int st = 0; st < npre; ++st)
-                tma_stage(st, &p.maps.s13, &p.maps.s13s, fp4, (fp4 ? k0 / 2 : k0) + st * 128, k0 / 16 + st * 16,
-                          tile * 128, p.Is + tile * 128, 0, pol);
+                tma_stage(st, &p.maps.s13, &p.maps.s13s, fp4, (fp4 ? k00 / 2 : k00) + st * 128, k00 / 16 + st * 16,
+                          tile0 * 128, p.Is + tile0 * 128, 0, pol);
         }
     }
+    if (warp != 1) griddep_wait();
+    // A chained launch may have started under the previous kernel on the
+    // stream: up to here it has touched only its own shared memory, TMEM and
+    // constant weights. Inputs and the workspace are read after the previous
+    // grid has completed.
     uint32_t start_no = 0;
     if (warp == 1) {
         tmem_alloc(tmem_base_s, kTmemCols);
         tc_fence_before();
+        griddep_wait();
         // this launch's parity: CTA starts are counted modulo 2 * grid (the
         // result is used after the conversion's loads are in flight)
         if (lane == 0) start_no = atomicInc(&p.hdr->start_cnt, 2u * gridDim.x - 1u);
@@ -392,7 +478,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
             comb_w[j + t + 1] = __ldg(p.topk_w + j);  // [t][1 + q]
         }
     }
-    if (warp >= 1) tc_convert_x(p, (tid - 32) * (int)gridDim.x + (int)blockIdx.x, nw1 * (int)gridDim.x);
+    bool shifted = false;
+    if (warp >= 1) shifted = tc_convert_rows(p, tid - 32, nw1, 3, reinterpret_cast<uint32_t *>(smem + TcSmem::red));
     if (tid == 32) *par_s = (int)(start_no / gridDim.x);
 
     // routed launches: warps 1.. of every CTA compute their share of the
@@ -435,12 +522,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
     if (warp >= 1) {
         group_table_cta(nullptr, T, K, p.E, no_dedup, tab, gt_scr, blockIdx.x == 0 ? err : nullptr, 32, nw1, 1);
         if (tid == 32) {  // the table's barriers ordered this CTA's activation stores
+            if (shifted) atomicOr(&p.hdr->x_scaled[*par_s], 1u);
             __threadfence();
             red_add_release_gpu(&p.hdr->x_ready[*par_s], 1u);
         }
     }
     __syncthreads();
     tc_fence_after();
+    griddep_launch_dependents();  // a chained next launch may now take each SM this grid leaves
     const int G = tab.G();
     const int32_t *gexp = tab.gexp(), *gn = tab.gncols(), *g0 = tab.gcol0(), *rcol = tab.row_col();
     const int *crow = tab.col_row();
@@ -506,13 +595,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
         {
             const int opar = par ^ 1;
             const int gt = (int)blockIdx.x * nw1 + (tid - 32);
-            const int nz = kTcReadyCap + kTcHtileCap + 3;
+            const int nz = kTcReadyCap + kTcHtileCap + 4;
             for (int i = gt; i < nz; i += nw1 * (int)gridDim.x) {
                 if (i < kTcReadyCap) p.group_ready[opar * kTcReadyCap + i] = 0u;
                 else if (i < kTcReadyCap + kTcHtileCap) p.htile_cnt[opar * kTcHtileCap + i - kTcReadyCap] = 0u;
                 else if (i == kTcReadyCap + kTcHtileCap) p.hdr->job_next[opar] = 0u;
                 else if (i == kTcReadyCap + kTcHtileCap + 1) p.hdr->x_ready[opar] = 0u;
-                else p.hdr->route_ready[opar] = 0u;
+                else if (i == kTcReadyCap + kTcHtileCap + 2) p.hdr->route_ready[opar] = 0u;
+                else p.hdr->x_scaled[opar] = 0u;
             }
         }
     }
@@ -643,6 +733,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                     const unsigned long long t0 = globaltimer_ns();
                     while (!mbar_try_wait(&rfull[s], par) && globaltimer_ns() - t0 < kWaitBudgetNs) {
                     }
+                }
+            }
+        }
+        // Every job is claimed: while this launch drains and combines, the
+        // stages that CTA b of the next launch (same shape, the next layer's
+        // shared expert) requests first are brought into L2, so they arrive
+        // from L2 instead of HBM when that launch starts.
+        __syncwarp();
+        if (p.nx13 && !*abort_flag) {
+            int tile = 0, k0 = 0;
+            const int n = tc_first_stages(p, no_dedup, nR, &tile, &k0);
+            if (n) {
+                const bool fp4 = p.shared.fmt == kFmtNvfp4;
+                const size_t rb = fp4 ? (size_t)H / 2 : (size_t)H, sb = (size_t)H / 16;  // bytes per row
+                for (int r = lane; r < 256; r += 32) {
+                    const size_t row = (size_t)(r < 128 ? tile * 128 + r : p.Is + tile * 128 + (r - 128));
+                    prefetch_l2_bulk(p.nx13 + row * rb + (fp4 ? k0 / 2 : k0), (uint32_t)n * 128u);
+                    if (fp4) prefetch_l2_bulk(p.nx13s + row * sb + k0 / 16, (uint32_t)n * 16u);
                 }
             }
         }
@@ -944,6 +1052,33 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
             __syncwarp();
             if (lane == 0) mbar_arrive(coef_bar);
         }
+        // the rows' activation scale exponents into shared memory, once every
+        // CTA's share of the activations is converted, by the first epilogue
+        // warp (idle until the first MMAs complete); xs_s[T] holds 1 when some
+        // row is shifted, so launches without shifted rows skip the rescaling
+        if (warp == 2 + kIssuers + kDqWarps) {
+            int okx = 1;
+            if (lane == 0) {
+                const unsigned long long t0 = globaltimer_ns();
+                while (ld_acquire_gpu(&p.hdr->x_ready[par]) < gridDim.x) {
+                    if (*abort_flag || globaltimer_ns() - t0 > kWaitBudgetNs) {
+                        if (!*abort_flag) atomicOr(err, kErrWaitTimeout);
+                        *abort_flag = 1;
+                        okx = 0;
+                        break;
+                    }
+                    __nanosleep(128);
+                }
+            }
+            okx = __shfl_sync(0xffffffffu, okx, 0);
+            const int any = okx ? (int)__ldcg(&p.hdr->x_scaled[par]) : 0;
+            for (int t = lane; t < T; t += 32) xs_s[t] = any ? __ldcg(p.xs + t) : 0;
+            if (lane == 0) xs_s[T] = any ? 1 : 0;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(xs_bar);
+        }
+        (void)__all_sync(0xffffffffu, mbar_wait(xs_bar, 0, abort_flag, err));
+        const bool xsc = xs_s[T] != 0;  // some activation row is shifted
         // fault injection (MOE_FLAG_DEBUG_DROP_ARRIVE): CTA 0's first quarter
         // skips its first intermediate-ready arrival, so the down jobs of that
         // (group, column tile) wait out their budget and the launch aborts
@@ -990,7 +1125,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                             p.P[(((size_t)d.kc * 2 + 0) * p.Ucap + col) * p.Imax + i] = v0;
                             p.P[(((size_t)d.kc * 2 + 1) * p.Ucap + col) * p.Imax + i] = v1;
                         } else {
-                            const float m = __fmul_rn(silu_f32(__fmul_rn(v0, gs13)), __fmul_rn(v1, gs13));
+                            const int sx = xsc ? xs_s[crow[col]] : 0;
+                            const float m = swiglu_scaled(__fmul_rn(v0, gs13), __fmul_rn(v1, gs13), pow2f(sx), pow2f(-sx));
                             const __half hm = __float2half_rn(m);
                             if (__hisinf(hm) || !(fabsf(m) == fabsf(m))) range_bad = 1;
                             *reinterpret_cast<__half *>(mb + b_off(c, r)) = hm;
@@ -1013,18 +1149,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                 const int rows = d.kind == 0 ? 2 * d.Ig : H;
                 const int cols_blk = (d.kind == 0 ? H : d.Ig) / 128;
                 const size_t sbase = (size_t)d.e * (rows / 128);
+                // the two tiles' block scales of a unit, loaded one unit ahead so
+                // the load is off the path from the unit's MMAs to the D release
+                const float *sc0 = sc + (sbase + d.rows0 / 128) * cols_blk + d.k0 / kUnitK;
+                const float *sc1 = sc + (sbase + d.rows1 / 128) * cols_blk + d.k0 / kUnitK;
+                const bool has1 = d.rows1 < rows;
+                float s0n = __ldg(sc0), s1n = has1 ? __ldg(sc1) : 0.0f;
                 for (int u = 0; u < d.nunits; ++u) {
+                    const float s0 = s0n, s1 = s1n;
+                    if (u + 1 < d.nunits) {
+                        s0n = __ldg(sc0 + u + 1);
+                        s1n = has1 ? __ldg(sc1 + u + 1) : 0.0f;
+                    }
                     if (!__all_sync(0xffffffffu, mbar_wait(&dfull[ds], dph, abort_flag, err))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const int ku = d.k0 / kUnitK + u;
-                    const float s0 = __ldg(sc + (sbase + d.rows0 / 128) * cols_blk + ku);
-                    const float s1 = (d.rows1 < rows) ? __ldg(sc + (sbase + d.rows1 / 128) * cols_blk + ku) : 0.0f;
                     const uint32_t dcol = tmem + lane_base + dcol0 + ds * dset;
 #pragma unroll
                     for (int h8 = 0; h8 < 16; h8 += 8) {
+                        if (h8 >= d.n) break;  // columns past the job's last one stay 0
                         uint32_t x0[8], x1[8];
                         tmem_ld8(dcol + h8, x0);
                         tmem_ld8(dcol + ntmax + h8, x1);
@@ -1095,7 +1240,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                                 sg = __fadd_rn(sg, __ldcg(p.P + (((size_t)kc * 2 + 0) * p.Ucap + col) * p.Imax + i));
                                 su = __fadd_rn(su, __ldcg(p.P + (((size_t)kc * 2 + 1) * p.Ucap + col) * p.Imax + i));
                             }
-                            const float m = __fmul_rn(silu_f32(__fmul_rn(sg, gs13)), __fmul_rn(su, gs13));
+                            const int sx = xsc ? xs_s[crow[col]] : 0;
+                            const float m = swiglu_scaled(__fmul_rn(sg, gs13), __fmul_rn(su, gs13), pow2f(sx), pow2f(-sx));
                             const __half hm = __float2half_rn(m);
                             if (__hisinf(hm) || !(fabsf(m) == fabsf(m))) range_bad = 1;
                             *reinterpret_cast<__half *>(mb + b_off(c, r)) = hm;
@@ -1167,7 +1313,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
             __nanosleep(128);
         }
         __syncwarp();
-    } else if (!*abort_flag && __all_sync(0xffffffffu, mbar_wait(coef_bar, 0, abort_flag, err))) {
+    } else if (!*abort_flag && __all_sync(0xffffffffu, mbar_wait(coef_bar, 0, abort_flag, err)) &&
+               __all_sync(0xffffffffu, mbar_wait(xs_bar, 0, abort_flag, err))) {
         const int ncw = kTcThreads / 32 - 1, hw = H / 32;  // combine warps 1..
         const long long nwu = (long long)T * hw;
         const int nkc_s = tc_nkc_dn(p.Is, T), nkc_r = tc_nkc_dn(p.I, T);
@@ -1190,6 +1337,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
             }
             const int32_t *rc = rcol + t * (K + 1);
             const float *cw = comb_w + t * (K + 1), *cg = comb_g + t * (K + 1);
+            const float fx = pow2f(2 * xs_s[t]);  // undoes the row's activation scale, squared (1 unless shifted)
             float y = 0.0f;
             int lq = 0, lk = 0;  // (slot, chunk) of the next term to load
             int aq = 0, ak = 0;  // ... and to add
@@ -1213,7 +1361,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                         const int nk = aq == 0 ? nkc_s : nkc_r;
                         y = ak == 0 ? v[u] : __fadd_rn(y, v[u]);
                         if (ak == nk - 1) {
-                            if (rc[aq] >= 0) acc = __fmaf_rn(cw[aq], __fmul_rn(y, cg[aq]), acc);
+                            if (rc[aq] >= 0) acc = __fmaf_rn(cw[aq], __fmul_rn(__fmul_rn(y, cg[aq]), fx), acc);
                             ak = 0;
                             ++aq;
                         } else {

@@ -50,7 +50,8 @@ struct WsHeader {
     uint32_t job_next[2];  // tensor-core path, per parity: jobs claimed past the first round
     uint32_t x_ready[2];   // tensor-core path, per parity: CTAs done converting their activation slice
     uint32_t route_ready[2];  // tensor-core path, per parity: CTAs done with their router partial logits
-    uint32_t pad[54];
+    uint32_t x_scaled[2];  // tensor-core path, per parity: nonzero when some activation row is shifted
+    uint32_t pad[52];
 };
 static_assert(sizeof(WsHeader) == 256, "header size");
 

@@ -16,6 +16,26 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// ---- programmatic dependent launch ---------------------------------------
+// A grid launched with programmatic stream serialization may start while the
+// previous kernel on its stream still runs; griddep_wait() blocks the calling
+// thread until that grid has completed and its writes are visible (it returns
+// at once for a grid launched without the attribute). griddep_launch_dependents()
+// lets such a dependent grid be scheduled once every CTA of this grid has
+// issued it or exited.
+
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Requests `bytes` (a multiple of 16) at a 16-byte-aligned global address
+// into L2, with no completion to wait for.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // ---- mbarrier ------------------------------------------------------------
 
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {

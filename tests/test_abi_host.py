@@ -51,6 +51,13 @@ def test_workspace_bytes_grow_with_T_and_reject_bad_shapes():
         assert B.moe_workspace_bytes(_shape(**bad)) == 0, bad
 
 
+def test_every_declared_flag_is_accepted_and_leaves_the_workspace_size():
+    base = B.moe_workspace_bytes(_shape(T=8))
+    for f in (B.MOE_FLAG_NO_DEDUP, B.MOE_FLAG_FORCE_FMA, B.MOE_FLAG_FORCE_MMA, B.MOE_FLAG_DEBUG_DROP_ARRIVE,
+              B.MOE_FLAG_CHAIN, B.MOE_FLAG_CHAIN | B.MOE_FLAG_FORCE_MMA):
+        assert B.moe_workspace_bytes(_shape(T=8, flags=f)) == base, f
+
+
 def test_workspace_bytes_never_shrink_as_T_grows():
     # the header states that a workspace sized for T serves every smaller T;
     # the tensor path's K-chunk partials change shape at T=3 and T=17
@@ -132,3 +139,22 @@ def test_host_call_rejects_small_workspace():
     st = B.lib().moe_fused_decode_host(1, 1, 1, ctypes.byref(_weights()), ctypes.byref(_weights()),
                                        1, ctypes.byref(s), ws.addr, ws.n, 0)
     assert st == B.MOE_ERR_WORKSPACE
+
+
+def test_next_layer_hint_is_checked_before_any_launch():
+    """moe_fused_decode_next rejects a missing, incomplete, misaligned or
+    other-format next shared expert on the host, before the device is touched."""
+    s = _shape()
+    ws = _FakeTensor(1 << 30, B.moe_workspace_bytes(s))
+
+    def call(nxt):
+        ref = ctypes.byref(nxt) if nxt is not None else None
+        return B.lib().moe_fused_decode_next(1 << 24, 1 << 28, 1 << 29, ctypes.byref(_weights()),
+                                             ctypes.byref(_weights()), ref, 1 << 26, ctypes.byref(s),
+                                             ws.addr, ws.n, 0)
+
+    assert call(None) == B.MOE_ERR_INVALID_ARG
+    assert call(_weights(B.MOE_W_FP8_B128)) == B.MOE_ERR_INVALID_ARG      # another format than `shared`
+    assert "format" in B.lib().moe_last_error_detail().decode()
+    assert call(_weights(addr=(1 << 20) + 8)) == B.MOE_ERR_INVALID_ARG    # misaligned
+    assert call(B.moe_weights(B.MOE_W_BF16, None, None, None, 1 << 20, None, None)) == B.MOE_ERR_INVALID_ARG

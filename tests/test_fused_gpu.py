@@ -221,6 +221,29 @@ def test_negative_controls(path):
     assert rows_changed(run_fused(L, PATHS[path])) == set()
 
 
+ROW_SCALES = [1e-30, 1e-6, 1.0, 1e3, 1e6, 1e12, 1e15]
+
+
+@pytest.mark.parametrize("path", list(PATHS))
+def test_activation_rows_from_tiny_to_huge(path):
+    """Rows whose magnitudes span 1e-30 to 1e15 (the output grows like |x|^2,
+    so 1e15 is near the top of what bf16 can hold): every row matches the
+    oracle within the tolerance taken over that row alone, no device error bit
+    is set, and dedup stays bitwise equal to the one-row form."""
+    s = inputs.Shape(T=len(ROW_SCALES), H=512, I=256, I_shared=512, E=16, K=4)
+    L = layer(s, "uniform", seed=14, used_only=False)
+    sc = torch.tensor(ROW_SCALES, dtype=torch.float64, device="cuda")[:, None]
+    L.x = (L.x.double() * sc).to(torch.bfloat16)
+    out = run_fused(L, PATHS[path])  # asserts the device error word is 0
+    ref = oracle_ref(L)
+    got = out.float().cpu().double().numpy()
+    for r in range(s.T):
+        assert_parity(out[r:r + 1], ref[r:r + 1])
+    assert np.isfinite(got).all()
+    one_row = run_fused(L, PATHS[path] | B.MOE_FLAG_NO_DEDUP)
+    assert torch.equal(out.view(torch.int16), one_row.view(torch.int16))
+
+
 @pytest.mark.parametrize("path", list(PATHS))
 def test_zero_down_weights_give_residual(path):
     s = inputs.Shape(T=4, H=256, I=256, I_shared=256, E=8, K=2)

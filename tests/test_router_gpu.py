@@ -43,7 +43,7 @@ def key_error_bound(x, wr):
 
 def check_picks(ids, w, x, wr, bias, K, scale, renorm):
     """ids/w from the GPU; returns the number of rows whose picks had to be
-    judged inside the error band (0 means every pick was compared exactly)."""
+    checked inside the error band (0 means every pick was compared exactly)."""
     T, E = ids.shape[0], wr.shape[0]
     ref_ids, ref_w, keys = oracle.route(x, wr, bias, T, x.shape[1], E, K, scale=scale, renorm=renorm)
     delta = key_error_bound(x, wr)
