@@ -47,6 +47,7 @@ WORKLOADS = {
 # computed inside the same launch
 ROUTED = {"dsv3_t1_routed": dict(T=1)}
 N_COPIES = 4
+HEAD_START_CYCLES = 4_000_000  # device sleep (about 2 ms) before a back-to-back timed region
 KERNEL_SOURCES = ["moe_layer_decode_persistent_b300/csrc/api.cu",
                   "moe_layer_decode_persistent_b300/csrc/fused_fma.cuh",
                   "moe_layer_decode_persistent_b300/csrc/fused_tc.cuh",
@@ -242,26 +243,35 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize()
     assert B.moe_read_error(ws) == 0
 
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    # the timed region: K launches back to back between two events (a short
+    # device-side sleep ahead of the first event lets the host queue launches
+    # before the clock starts, so host launch latency does not open gaps)
     barrier(world)
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda._sleep(HEAD_START_CYCLES)
     t0.record(stream)
     for i in range(args.steps):
-        starts[i].record(stream)
         launch(i)
-        ends[i].record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     err = B.moe_read_error(ws)
-    per_launch = [s.elapsed_time(e) * 1e3 for s, e in zip(starts, ends)]  # us
     total_ms = t0.elapsed_time(t1)
     ms_per_step = max_over_ranks(total_ms / args.steps, world, dev)
-    us_launch = statistics.mean(per_launch)
-    us_launch_max = max_over_ranks(us_launch, world, dev)
+    us_launch_max = ms_per_step * 1e3
+
+    # the same launches once more with an event pair around each, for the
+    # spread of single launches (events between launches add their own gaps)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for i in range(args.steps):
+        starts[i].record(stream)
+        launch(i)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    per_launch = [s.elapsed_time(e) * 1e3 for s, e in zip(starts, ends)]  # us
 
     # end to end through the host-buffer entry point (pinned buffers, copies inside)
     if args.no_e2e:
@@ -393,6 +403,7 @@ def chain_ab(variants: dict, n_launch: int, rounds: int = 3, reps: int = 3) -> d
     def eager(f):
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(HEAD_START_CYCLES)
         a.record(st)
         for i in range(n_launch):
             f(i, st)
@@ -429,6 +440,23 @@ def chain_ab(variants: dict, n_launch: int, rounds: int = 3, reps: int = 3) -> d
     return out
 
 
+def back_to_back_us(launch, n: int) -> float:
+    """us per launch of n launches back to back on the current stream, between
+    two events."""
+    import torch
+    st = torch.cuda.current_stream()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    torch.cuda._sleep(HEAD_START_CYCLES)
+    a.record(st)
+    for i in range(n):
+        launch(i)
+    b.record(st)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) * 1e3 / n
+
+
 def sweep_point(name, args, dev):
     """us per launch for another workload (same protocol, fewer steps)."""
     import torch
@@ -451,15 +479,9 @@ def sweep_point(name, args, dev):
     for i in range(3):
         B.moe_fused_decode(L.x, L.topk_ids, L.topk_w, *weights[i % N_COPIES], out, sh, ws)
     n = max(20, args.steps // 2)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
-    torch.cuda.synchronize()
-    for i in range(n):
-        ev[i][0].record()
-        B.moe_fused_decode(L.x, L.topk_ids, L.topk_w, *weights[i % N_COPIES], out, sh, ws)
-        ev[i][1].record()
-    torch.cuda.synchronize()
+    us = back_to_back_us(lambda i: B.moe_fused_decode(L.x, L.topk_ids, L.topk_w, *weights[i % N_COPIES], out,
+                                                      sh, ws), n)
     assert B.moe_read_error(ws) == 0
-    us = statistics.mean(a.elapsed_time(b) * 1e3 for a, b in ev)
 
     def launch_s(i, s):
         B.moe_fused_decode(L.x, L.topk_ids, L.topk_w, *weights[i % N_COPIES], out, sh, ws, stream=s)
@@ -512,15 +534,8 @@ def routed_point(name, args, dev):
     for i in range(3):
         launch_s(i)
     n = max(20, args.steps // 2)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
-    torch.cuda.synchronize()
-    for i in range(n):
-        ev[i][0].record()
-        launch_s(i)
-        ev[i][1].record()
-    torch.cuda.synchronize()
+    us = back_to_back_us(launch_s, n)
     assert B.moe_read_error(ws) == 0
-    us = statistics.mean(a.elapsed_time(b) * 1e3 for a, b in ev)
     g_us = graph_us_per_launch(launch_s, 2 * N_COPIES)
     assert B.moe_read_error(ws) == 0
     distinct = len(set(ids.cpu().reshape(-1).tolist()))
@@ -577,6 +592,7 @@ def wide_sweep(args, dev, n_layers: int = 4):
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
+        torch.cuda._sleep(HEAD_START_CYCLES)
         a.record(stream)
         for i in range(n):
             launch_s(i, stream)
@@ -761,6 +777,9 @@ def main():
          "d2h_bytes_per_step": r["d2h"]},
         "gpu_launches": args.steps, "clocks": r["clocks"], "device_error_word": r["err"],
         "graph_us_per_launch": None if r["graph_us"] is None else round(r["graph_us"], 2),
+        "single_launch_us": {"median": round(statistics.median(r["per_launch"]), 2),
+                             "min": round(min(r["per_launch"]), 2), "max": round(max(r["per_launch"]), 2),
+                             "how": "an event pair around each launch, after the timed region"},
     }
     if r["chain"]:
         line["chain"] = r["chain"]

@@ -58,7 +58,7 @@ constexpr size_t kTcTileCntWords = (size_t)moe::kSplitMaxT * (kMaxK + 1) * (kMax
 struct WsLayout {
     size_t route = 0;  // router partial logits [T][E][kRouterParts] fp32 (routed launches)
     size_t mid = 0, y = 0, fma_end = 0;
-    size_t tc_ready = 0, tc_htile = 0, tc_tile = 0, tc_ctrl_end = 0, tc_P = 0, tc_Y = 0, tc_midB = 0,
+    size_t tc_ready = 0, tc_htile = 0, tc_tile = 0, tc_par = 0, tc_ctrl_end = 0, tc_P = 0, tc_Y = 0, tc_midB = 0,
            tc_xh = 0, tc_xs = 0, tc_end = 0;
     size_t dev_total = 0;
     size_t st_x = 0, st_ids = 0, st_w = 0, st_out = 0, host_total = 0;
@@ -80,6 +80,8 @@ WsLayout ws_layout(const moe_shape *s) {
     // Imax/128 row tiles; sized for the caps so the region never moves
     L.tc_tile = off = align_up(off, 16);
     off += kTcTileCntWords * 4;
+    L.tc_par = off = align_up(off, 16);  // one launch-parity word per CTA
+    off += (size_t)moe::kTcMaxGrid * 4;
     L.tc_ctrl_end = off = align_up(off, 256);
 
     L.mid = off;
@@ -500,6 +502,7 @@ moe_status launch_fused_tc(const moe::FusedParams &fp, const WsLayout &L, const 
     p.group_ready = reinterpret_cast<uint32_t *>(ws + L.tc_ready);
     p.tile_cnt = reinterpret_cast<uint32_t *>(ws + L.tc_tile);
     p.htile_cnt = reinterpret_cast<uint32_t *>(ws + L.tc_htile);
+    p.cta_par = reinterpret_cast<uint32_t *>(ws + L.tc_par);
     p.P = reinterpret_cast<float *>(ws + L.tc_P);
     p.Y = reinterpret_cast<float *>(ws + L.tc_Y);
     p.midB = reinterpret_cast<uint8_t *>(ws + L.tc_midB);
@@ -534,6 +537,9 @@ moe_status launch_fused_tc(const moe::FusedParams &fp, const WsLayout &L, const 
                      : (capped ? moe::fused_tc_kernel<true, false> : moe::fused_tc_kernel<false, false>);
     if ((st = plan_occupancy(kern, dev, moe::kTcThreads, smem, d, &occ)) != MOE_OK) return st;
     cudaLaunchConfig_t cfg = {};
+    if (d.nsm > moe::kTcMaxGrid)
+        return fail(MOE_ERR_UNSUPPORTED, "%d SMs: the tensor-core path keeps parity words for %d", d.nsm,
+                    moe::kTcMaxGrid);
     cfg.gridDim = dim3((unsigned)d.nsm);  // one CTA per SM: it holds all of TMEM
     cfg.blockDim = dim3(moe::kTcThreads);
     cfg.dynamicSmemBytes = smem;

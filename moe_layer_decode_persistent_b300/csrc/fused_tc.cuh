@@ -51,8 +51,9 @@
 //               warp as soon as its role is done
 //
 // Precision: weights dequantise exactly to f16 (e2m1*e4m3 has <= 6
-// significant bits); activations bf16 -> f16 (exact for |x| in [2^-17, 65504];
-// larger magnitudes set MOE_DEV_RANGE); the fp32 SwiGLU intermediate is
+// significant bits); activations bf16 -> f16, each row scaled by a power of
+// two that keeps its largest element below 16 (exact wherever f16 holds the
+// scaled value); the fp32 SwiGLU intermediate is
 // rounded once to f16 for the down MMA (relative error <= 2^-12 per element,
 // about 1.4e-4 |y| rms on the down output); every accumulation is fp32.
 #pragma once
@@ -104,6 +105,7 @@ constexpr int kCombBatch = 20;  // combine: partial sums loaded per batch (18 fo
 // Launch-wide counters, two sets used in alternate launches (by parity).
 constexpr int kTcReadyCap = 256 * 17;  // (group, column tile) pairs: at most T*(K+1)
 constexpr int kTcHtileCap = 64;        // 256-row output tiles: H / 256 at most
+constexpr int kTcMaxGrid = 1024;       // CTAs (SMs) a launch may have: one parity word each
 
 struct TcMaps {
     CUtensorMap r13, r13s, r2, r2s, s13, s13s, s2, s2s;
@@ -133,6 +135,7 @@ struct TcParams {
     uint32_t *group_ready;  // [2][kTcReadyCap], per parity, per (group, column tile)
     uint32_t *tile_cnt;     // per (group, column tile, 128-row tile); each launch leaves it zero
     uint32_t *htile_cnt;    // [2][kTcHtileCap], per parity, per 256-row output tile
+    uint32_t *cta_par;      // [kTcMaxGrid]: CTA b's parity of its next launch, toggled by CTA b alone
     float *P;               // gate/up partials [kc][2][Ucap][Imax]
     float *Y;               // down partials [kc][Ucap][H]
     uint8_t *midB;          // f16 intermediate in MMA B layout
@@ -244,16 +247,18 @@ __device__ __forceinline__ int group_of_col(const int32_t *g0, int G, int c) {
 // [2^-17, 65504]); a shifted row keeps f16's 11 bits for everything within
 // 2^-24 of its largest element. The gate/up epilogue undoes the shift inside
 // the SwiGLU and the combine undoes its square, so results are unchanged
-// except where f16 would have overflowed (MOE_DEV_RANGE now only for
-// non-finite inputs or intermediates).
+// except where f16 would have overflowed (MOE_DEV_RANGE is left for
+// non-finite inputs and intermediates).
 //
 // Rows are shared out over the CTAs: with T < grid, the CTAs b = t + T*k
 // (k < grid / T) split row t's 16-byte items between them; with T >= grid,
 // CTA b converts rows b, b + grid, ... whole. Each CTA finds the maximum of
-// the rows it touches itself (a reduction over warps 1.. behind named barrier
-// `bar`), so the shift needs no exchange between CTAs; the CTA holding a
+// the rows it touches itself (a reduction over the converting warps behind
+// named barrier `bar`), so the shift needs no exchange between CTAs; the CTA holding a
 // row's first slice writes s_t.
 constexpr int kMaxActShift = 63;
+constexpr int kWarpTablePicks = 32;  // up to this many picks, warp 1 alone builds the group table
+constexpr int kWarpPicks = 128;      // up to this many picks, warp 1 alone loads them
 // The raw stages that CTA b requests before its group table is built: its
 // first job, when that is one of the shared expert's gate/up jobs (the shared
 // expert is group 0 in either form and its gate/up jobs come first in the
@@ -279,7 +284,7 @@ __device__ __forceinline__ int act_shift(uint32_t max_abs_bits) {
 }
 
 __device__ __forceinline__ bool tc_convert_rows(const TcParams &p, int tid1, int nthr1, int bar, uint32_t *red_s) {
-    constexpr int kMaxItems = 4;  // 16-byte items of a row a thread holds: H <= 16384, 17 warps
+    constexpr int kMaxItems = 4;  // 16-byte items of a row a thread holds: H <= 16384, 16 warps
     const int T = p.T, G = (int)gridDim.x, b = (int)blockIdx.x;
     const int n8 = p.H / 8;  // 16-byte items per row
     const int nsl = T < G ? G / T : 1;  // CTAs per row
@@ -338,11 +343,20 @@ __device__ __forceinline__ bool tc_convert_rows(const TcParams &p, int tid1, int
     if (range_bad) atomicOr(&p.hdr->err, kErrRange);
     return shifted;
 }
-static_assert(16384 / 8 <= 4 * (kTcThreads - 32), "a row's items fit the converting threads' registers");
+static_assert(16384 / 8 <= 4 * (kTcThreads - 64), "a row's items fit the converting threads' registers");
 
 // SwiGLU of a column whose activations were scaled by 2^-s (g, u: the scaled
 // gate and up sums, global scales applied; fs = 2^s, fis = 2^-s): the true
 // silu(g 2^s) (u 2^s), scaled by 2^-2s. With s = 0 it is silu(g) u exactly.
+// This CTA's slice of the activations (and its shifted-row flag) goes out to
+// the grid: a release after the barrier that ordered the converting warps'
+// stores.
+__device__ __forceinline__ void tc_publish_x(const TcParams &p, int par, bool shifted) {
+    if (shifted) atomicOr(&p.hdr->x_scaled[par], 1u);
+    __threadfence();
+    red_add_release_gpu(&p.hdr->x_ready[par], 1u);
+}
+
 __device__ __forceinline__ float swiglu_scaled(float g, float u, float fs, float fis) {
     return __fmul_rn(__fmul_rn(silu_f32(__fmul_rn(g, fs)), fis), u);
 }
@@ -380,6 +394,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + TcSmem::misc + 4);
     int *dn_per_ht_s = reinterpret_cast<int *>(smem + TcSmem::misc + 8);
     int *par_s = reinterpret_cast<int *>(smem + TcSmem::misc + 12);
+    int *shifted_s = reinterpret_cast<int *>(smem + TcSmem::misc + 16);  // some row of this CTA's share is shifted
     uint32_t *tile_ready_s = reinterpret_cast<uint32_t *>(smem + TcSmem::tile_ready);
     int32_t *tbl = reinterpret_cast<int32_t *>(smem + TcSmem::tables);
     GroupTable tab{tbl, C, gcap};
@@ -458,29 +473,66 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
     // grid has completed.
     uint32_t start_no = 0;
     if (warp == 1) {
+        griddep_wait();
+        // this launch's parity: every CTA keeps its own word, flipped once per
+        // launch, so all CTAs of a launch read the same value without a shared
+        // counter (148 CTAs on one address cost microseconds). Only tid 32
+        // uses it, when it publishes this CTA's activations, so the load's
+        // round trip overlaps the TMEM allocation, the conversion and the
+        // group table.
+        if (lane == 0) {
+            uint32_t *cp = p.cta_par + blockIdx.x;
+            start_no = __ldcg(cp);
+            __stcg(cp, start_no ^ 1u);
+        }
+        __syncwarp();
         tmem_alloc(tmem_base_s, kTmemCols);
         tc_fence_before();
-        griddep_wait();
-        // this launch's parity: CTA starts are counted modulo 2 * grid (the
-        // result is used after the conversion's loads are in flight)
-        if (lane == 0) start_no = atomicInc(&p.hdr->start_cnt, 2u * gridDim.x - 1u);
     }
     int *gt_scr = reinterpret_cast<int *>(raw + (nR - 1) * kRawStageBytes);  // group table scratch
-    // The step's picks and router weights come first, in the same round trip
-    // as the activations and ahead of the weight stream: the picks into the
-    // group table's scratch, the weights into the pick slots of the combine
-    // weights (a routed launch computes both on chip below).
-    if (warp >= 1 && !kRouted) {
+    // The step's picks and router weights go first, ahead of the conversion
+    // and the weight stream: the picks into the group table's scratch, the
+    // weights into the pick slots of the combine weights (a routed launch
+    // computes both on chip below). Up to kWarpPicks picks, warp 1 alone
+    // loads them (warps 2.. start converting at once); up to kWarpTablePicks,
+    // warp 1 also builds the group table while warps 2.. convert (the table
+    // is short, once-per-launch code whose instruction fetches dominate it);
+    // above, warps 1.. share both, the table after the conversion.
+    const bool warp_table = !kRouted && T * K <= kWarpTablePicks;
+    const int nT = warp_table ? 32 : nw1;  // threads that build the table
+    if (!kRouted && T * K <= kWarpPicks) {
+        if (warp == 1) {  // all loads in flight at once, then the stores
+            int32_t *picks = group_table_picks(gt_scr, p.E);
+            int32_t v[kWarpPicks / 32];
+            float w[kWarpPicks / 32];
+#pragma unroll
+            for (int r = 0; r < kWarpPicks / 32; ++r) {
+                const int j = lane + 32 * r;
+                v[r] = j < T * K ? __ldg(p.ids + j) : 0;
+                w[r] = j < T * K ? __ldg(p.topk_w + j) : 0.0f;
+            }
+#pragma unroll
+            for (int r = 0; r < kWarpPicks / 32; ++r) {
+                const int j = lane + 32 * r;
+                if (j < T * K) {
+                    picks[j] = v[r];
+                    comb_w[j + j / K + 1] = w[r];  // [t][1 + q]
+                }
+            }
+        }
+    } else if (!kRouted && warp >= 1) {
         int32_t *picks = group_table_picks(gt_scr, p.E);
         for (int j = tid - 32; j < T * K; j += nw1) {
-            const int t = j / K;
             picks[j] = __ldg(p.ids + j);
-            comb_w[j + t + 1] = __ldg(p.topk_w + j);  // [t][1 + q]
+            comb_w[j + j / K + 1] = __ldg(p.topk_w + j);
         }
     }
-    bool shifted = false;
-    if (warp >= 1) shifted = tc_convert_rows(p, tid - 32, nw1, 3, reinterpret_cast<uint32_t *>(smem + TcSmem::red));
-    if (tid == 32) *par_s = (int)(start_no / gridDim.x);
+    // warps 2.. convert (warp 1 allocates TMEM, reads the parity and builds
+    // a small table meanwhile, so the row maxima's barrier does not wait for it)
+    if (warp >= 2) {
+        const bool shifted = tc_convert_rows(p, tid - 64, nw1 - 32, 3, reinterpret_cast<uint32_t *>(smem + TcSmem::red));
+        if (tid == 64) *shifted_s = shifted ? 1 : 0;  // read after the CTA barrier below
+    }
 
     // routed launches: warps 1.. of every CTA compute their share of the
     // router's partial logits (warp 0 streams the first weights meanwhile),
@@ -494,7 +546,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
         named_bar_sync(2, nw1);
         if (tid == 32) {
             __threadfence();
-            uint32_t *rr = &p.hdr->route_ready[*par_s];
+            uint32_t *rr = &p.hdr->route_ready[start_no];
             red_add_release_gpu(rr, 1u);
             const unsigned long long t0 = globaltimer_ns();
             while (ld_acquire_gpu(rr) < gridDim.x) {
@@ -515,21 +567,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
         }
     }
 
-    // the group table, by warps 1.. behind named barrier 1 (warp 0 streams
-    // meanwhile; the table's scratch is the raw ring's last stage); then this
-    // CTA's slice of the activations is published, and one CTA barrier
-    // publishes the mbarriers, the TMEM address, the parity and the table
-    if (warp >= 1) {
-        group_table_cta(nullptr, T, K, p.E, no_dedup, tab, gt_scr, blockIdx.x == 0 ? err : nullptr, 32, nw1, 1);
-        if (tid == 32) {  // the table's barriers ordered this CTA's activation stores
-            if (shifted) atomicOr(&p.hdr->x_scaled[*par_s], 1u);
-            __threadfence();
-            red_add_release_gpu(&p.hdr->x_ready[*par_s], 1u);
-        }
+    // the group table, by the threads that loaded the picks, behind named
+    // barrier 1 (warp 0 streams meanwhile; the table's scratch is the raw
+    // ring's last stage); one CTA barrier then publishes the mbarriers, the
+    // TMEM address, the parity, the table and this CTA's activation slice
+    if (warp >= 1 && tid - 32 < nT)
+        group_table_cta(nullptr, T, K, p.E, no_dedup, tab, gt_scr, blockIdx.x == 0 ? err : nullptr, 32, nT, 1);
+    // This CTA's activation slice goes out to the grid from tid 32 once a
+    // barrier has ordered the converting warps' stores: with a one-warp table
+    // after the CTA barrier (so no warp waits for the fence), else right after
+    // the table's own barriers, which the converting warps take part in.
+    if (tid == 32) {
+        *par_s = (int)start_no;
+        if (!warp_table) tc_publish_x(p, (int)start_no, *shifted_s != 0);
     }
     __syncthreads();
     tc_fence_after();
     griddep_launch_dependents();  // a chained next launch may now take each SM this grid leaves
+    if (tid == 32 && warp_table) tc_publish_x(p, (int)start_no, *shifted_s != 0);
     const int G = tab.G();
     const int32_t *gexp = tab.gexp(), *gn = tab.gncols(), *g0 = tab.gcol0(), *rcol = tab.row_col();
     const int *crow = tab.col_row();

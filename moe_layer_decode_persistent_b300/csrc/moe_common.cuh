@@ -46,7 +46,7 @@ struct WsHeader {
     uint32_t err;          // device error word (MOE_DEV_* bits)
     uint32_t bar_count;    // grid barrier: arrivals in the current round
     uint32_t bar_gen;      // grid barrier: completed rounds (monotonic)
-    uint32_t start_cnt;    // tensor-core path: CTA starts modulo 2*grid; start_cnt / grid = launch parity
+    uint32_t spare;        // unused
     uint32_t job_next[2];  // tensor-core path, per parity: jobs claimed past the first round
     uint32_t x_ready[2];   // tensor-core path, per parity: CTAs done converting their activation slice
     uint32_t route_ready[2];  // tensor-core path, per parity: CTAs done with their router partial logits
