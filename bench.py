@@ -275,10 +275,13 @@ def run_ours(args, rank, world, local):
 
     # end to end through the host-buffer entry point (pinned buffers, copies inside)
     if args.no_e2e:
+        del copies, weights
+        torch.cuda.empty_cache()
+        wide = wide_sweep(args, dev) if args.sweep_wide else {}
         clk.__exit__()
         return dict(us_launch=us_launch_max, ms_per_step=ms_per_step, algo_bytes=algo_bytes,
                     distinct=distinct, clocks=clk.summary(), err=err, e2e_us=None, h2d=0, d2h=0,
-                    sweep={}, wide={}, graph_us=None, T=shape.T, per_launch=per_launch, chain=None)
+                    sweep={}, wide=wide, graph_us=None, T=shape.T, per_launch=per_launch, chain=None)
     xh = L.x.cpu().pin_memory()
     ih = L.topk_ids.cpu().pin_memory()
     wh = L.topk_w.cpu().pin_memory()

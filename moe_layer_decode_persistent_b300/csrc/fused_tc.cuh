@@ -476,10 +476,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
         griddep_wait();
         // this launch's parity: every CTA keeps its own word, flipped once per
         // launch, so all CTAs of a launch read the same value without a shared
-        // counter (148 CTAs on one address cost microseconds). Only tid 32
-        // uses it, when it publishes this CTA's activations, so the load's
-        // round trip overlaps the TMEM allocation, the conversion and the
-        // group table.
+        // counter. Only tid 32 uses it, when it publishes this CTA's
+        // activations, so the load's round trip overlaps the TMEM allocation,
+        // the picks and the conversion.
         if (lane == 0) {
             uint32_t *cp = p.cta_par + blockIdx.x;
             start_no = __ldcg(cp);
