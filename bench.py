@@ -234,9 +234,37 @@ def run_ours(args, rank, world, local):
         rw, sw = weights[i % len(weights)]
         B.moe_fused_decode(L.x, L.topk_ids, L.topk_w, rw, sw, out, sh, ws, stream=stream)
 
+    # End to end through the host-buffer entry point (pinned buffers, copies
+    # inside), before the clock sampler has ever run in this process: once
+    # nvidia-smi has run, this synchronous loop measured 151 us a step
+    # instead of 97 us for the rest of the process.
+    e2e_us = None
+    if not args.no_e2e:
+        xh = L.x.cpu().pin_memory()
+        ih = L.topk_ids.cpu().pin_memory()
+        wh = L.topk_w.cpu().pin_memory()
+        oh = torch.empty_like(xh).pin_memory()
+
+        def launch_host(i):
+            rw, sw = weights[i % len(weights)]
+            B.moe_fused_decode_host(xh, ih, wh, rw, sw, oh, sh, ws, stream=stream)
+
+        for i in range(max(3, args.warmup)):
+            launch_host(i)
+        barrier(world)
+        h0 = time.perf_counter()
+        for i in range(args.steps):
+            launch_host(i)
+        e2e_us = (time.perf_counter() - h0) / args.steps * 1e6
+        e2e_us = max_over_ranks(e2e_us, world, dev)
+        launch(0)  # the device entry on the same inputs gives the same bits
+        torch.cuda.synchronize()
+        assert torch.equal(oh.view(torch.int16), out.cpu().view(torch.int16))
+
     # the clock sampler starts before the warm-up (its start-up pause would
-    # otherwise leave the GPU idle right before the timed region) and runs
-    # until the last GPU timing of this bench
+    # otherwise leave the GPU idle right before the timed region) and stops
+    # after the device-timed launches; a second sampler covers the graph,
+    # chained and sweep timings
     clk = ClockSampler(local).__enter__()
     for i in range(args.warmup):
         launch(i)
@@ -272,34 +300,20 @@ def run_ours(args, rank, world, local):
         ends[i].record(stream)
     torch.cuda.synchronize()
     per_launch = [s.elapsed_time(e) * 1e3 for s, e in zip(starts, ends)]  # us
+    clk.__exit__()
 
     # end to end through the host-buffer entry point (pinned buffers, copies inside)
     if args.no_e2e:
         del copies, weights
         torch.cuda.empty_cache()
+        clk2 = ClockSampler(local).__enter__()
         wide = wide_sweep(args, dev) if args.sweep_wide else {}
-        clk.__exit__()
+        clk2.__exit__()
         return dict(us_launch=us_launch_max, ms_per_step=ms_per_step, algo_bytes=algo_bytes,
                     distinct=distinct, clocks=clk.summary(), err=err, e2e_us=None, h2d=0, d2h=0,
-                    sweep={}, wide=wide, graph_us=None, T=shape.T, per_launch=per_launch, chain=None)
-    xh = L.x.cpu().pin_memory()
-    ih = L.topk_ids.cpu().pin_memory()
-    wh = L.topk_w.cpu().pin_memory()
-    oh = torch.empty_like(xh).pin_memory()
-
-    def launch_host(i):
-        rw, sw = weights[i % len(weights)]
-        B.moe_fused_decode_host(xh, ih, wh, rw, sw, oh, sh, ws, stream=stream)
-
-    for i in range(max(3, args.warmup)):
-        launch_host(i)
-    barrier(world)
-    h0 = time.perf_counter()
-    for i in range(args.steps):
-        launch_host(i)
-    e2e_us = (time.perf_counter() - h0) / args.steps * 1e6
-    e2e_us = max_over_ranks(e2e_us, world, dev)
-    assert torch.equal(oh.view(torch.int16), out.cpu().view(torch.int16))
+                    sweep={}, wide=wide, graph_us=None, T=shape.T, per_launch=per_launch, chain=None,
+                    clocks_after=clk2.summary() if args.sweep_wide else None)
+    clk2 = ClockSampler(local).__enter__()
 
     def launch_s(i, s):
         rw, sw = weights[i % len(weights)]
@@ -343,11 +357,12 @@ def run_ours(args, rank, world, local):
         for name in ROUTED:
             sweep[name] = routed_point(name, args, dev)
     wide = wide_sweep(args, dev) if args.sweep_wide else {}
-    clk.__exit__()
+    clk2.__exit__()
     return dict(us_launch=us_launch_max, ms_per_step=ms_per_step, algo_bytes=algo_bytes,
                 distinct=distinct, clocks=clk.summary(), err=err, e2e_us=e2e_us,
                 h2d=xh.numel() * 2 + ih.numel() * 4 + wh.numel() * 4, d2h=oh.numel() * 2,
-                sweep=sweep, wide=wide, graph_us=graph_us, T=shape.T, per_launch=per_launch, chain=chain)
+                sweep=sweep, wide=wide, graph_us=graph_us, T=shape.T, per_launch=per_launch, chain=chain,
+                clocks_after=clk2.summary())
 
 
 def graph_us_per_launch(launch, n_launch: int, reps: int = 5) -> float:
@@ -784,6 +799,8 @@ def main():
                              "min": round(min(r["per_launch"]), 2), "max": round(max(r["per_launch"]), 2),
                              "how": "an event pair around each launch, after the timed region"},
     }
+    if r.get("clocks_after"):
+        line["clocks_after_timed_region"] = r["clocks_after"]  # graph, chained and sweep timings
     if r["chain"]:
         line["chain"] = r["chain"]
     if r["sweep"]:
