@@ -310,14 +310,26 @@ def test_dropped_arrival_times_out_and_workspace_recovers(path):
     assert torch.equal(again.view(torch.int16), fresh.view(torch.int16))
 
 
-def test_host_buffer_entry_matches_device_entry():
-    L = layer(inputs.dsv3(8), "mtp", seed=9)
+@pytest.mark.parametrize("T,pinned", [
+    (8, "all"),        # page-locked host buffers (asynchronous copies)
+    (8, "none"),       # pageable host buffers
+    (1, "mixed"),      # some of each
+    (20, "all"),
+])
+def test_host_buffer_entry_matches_device_entry(T, pinned):
+    L = layer(inputs.dsv3(T), "mtp" if T == 8 else "uniform", seed=9)
     dev = run_fused(L, 0)
     ws = workspace(L, host=True)
-    xh = L.x.cpu().pin_memory()
-    ih = L.topk_ids.cpu().pin_memory()
-    wh = L.topk_w.cpu().pin_memory()
-    oh = torch.empty_like(xh).pin_memory()
+
+    def host(t, pin):
+        t = t.cpu().clone()
+        return t.pin_memory() if pin else t
+
+    xh = host(L.x, pinned != "none")
+    ih = host(L.topk_ids, pinned != "none")
+    wh = host(L.topk_w, pinned == "all")
+    oh = host(torch.empty_like(L.x), pinned != "none")
+    oh.fill_(7)
     B.moe_fused_decode_host(xh, ih, wh, B.make_weights(L.routed), B.make_weights(L.shared), oh,
                             shape_of(L), ws)
     assert torch.equal(oh.view(torch.int16), dev.cpu().view(torch.int16))
