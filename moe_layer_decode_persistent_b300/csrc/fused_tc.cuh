@@ -345,9 +345,6 @@ __device__ __forceinline__ bool tc_convert_rows(const TcParams &p, int tid1, int
 }
 static_assert(16384 / 8 <= 4 * (kTcThreads - 64), "a row's items fit the converting threads' registers");
 
-// SwiGLU of a column whose activations were scaled by 2^-s (g, u: the scaled
-// gate and up sums, global scales applied; fs = 2^s, fis = 2^-s): the true
-// silu(g 2^s) (u 2^s), scaled by 2^-2s. With s = 0 it is silu(g) u exactly.
 // This CTA's slice of the activations (and its shifted-row flag) goes out to
 // the grid: a release after the barrier that ordered the converting warps'
 // stores.
@@ -357,6 +354,9 @@ __device__ __forceinline__ void tc_publish_x(const TcParams &p, int par, bool sh
     red_add_release_gpu(&p.hdr->x_ready[par], 1u);
 }
 
+// SwiGLU of a column whose activations were scaled by 2^-s (g, u: the scaled
+// gate and up sums, global scales applied; fs = 2^s, fis = 2^-s): the true
+// silu(g 2^s) (u 2^s), scaled by 2^-2s. With s = 0 it is silu(g) u exactly.
 __device__ __forceinline__ float swiglu_scaled(float g, float u, float fs, float fis) {
     return __fmul_rn(__fmul_rn(silu_f32(__fmul_rn(g, fs)), fis), u);
 }
