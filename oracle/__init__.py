@@ -70,6 +70,10 @@ def lib():
         _lib.oracle_unfused_layer.argtypes = [p, p, p, p, p, i, i, i, i, i, i, p]
         _lib.oracle_moe_layer_uses.argtypes = [p, p, p, p, p, i, i, i, i, i, i, p, i, p, i]
         _lib.oracle_route.argtypes = [p, p, p, i, i, i, i, d, i, p, p, p]
+        _lib.oracle_e4m3_rne.restype = d
+        _lib.oracle_e4m3_rne.argtypes = [d]
+        _lib.oracle_fp8_mid_blocks.argtypes = [p, i, i]
+        _lib.oracle_moe_layer_fp8mid.argtypes = [p, p, p, p, p, i, i, i, i, i, i, p, i, p, i, i]
     return _lib
 
 
@@ -224,6 +228,37 @@ def moe_layer_uses(x_bf16, ids, topk_w, routed: WeightSet, shared: WeightSet, T,
     lib().oracle_moe_layer_uses(x.ctypes.data, ids.ctypes.data, w.ctypes.data, ctypes.byref(rs),
                                 ctypes.byref(ss), T, H, I, I_shared, E, K, rows.ctypes.data,
                                 len(rows), out.ctypes.data, int(threads))
+    return out
+
+
+FP8_MID_BLOCK = 32  # intermediate values per FP8 block (see oracle_fp8_mid_blocks)
+
+
+def e4m3_rne(v: float) -> float:
+    """The nearest E4M3FN value to v (ties to even), saturating at +-448."""
+    return lib().oracle_e4m3_rne(float(v))
+
+
+def fp8_mid_blocks(mid, block=FP8_MID_BLOCK) -> np.ndarray:
+    """A copy of mid with each block of `block` values quantised to E4M3 at
+    its power-of-two block scale (oracle_fp8_mid_blocks)."""
+    m = np.array(mid, np.float64, copy=True)
+    lib().oracle_fp8_mid_blocks(m.ctypes.data, len(m), int(block))
+    return m
+
+
+def moe_layer_fp8mid(x_bf16, ids, topk_w, routed: WeightSet, shared: WeightSet, T, H, I, I_shared, E, K,
+                     rows=None, threads=1, block=FP8_MID_BLOCK) -> np.ndarray:
+    """moe_layer with every expert use's SwiGLU intermediate in FP8 blocks."""
+    x = _np(x_bf16, np.uint16).reshape(-1)
+    ids = _np(ids, np.int32).reshape(-1)
+    w = _np(topk_w, np.float32).reshape(-1)
+    rows = np.arange(T, dtype=np.int32) if rows is None else np.ascontiguousarray(rows, np.int32)
+    out = np.empty((len(rows), H), np.float64)
+    rs, ss = routed.cstruct(), shared.cstruct()
+    lib().oracle_moe_layer_fp8mid(x.ctypes.data, ids.ctypes.data, w.ctypes.data, ctypes.byref(rs),
+                                  ctypes.byref(ss), T, H, I, I_shared, E, K, rows.ctypes.data,
+                                  len(rows), out.ctypes.data, int(threads), int(block))
     return out
 
 

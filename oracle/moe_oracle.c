@@ -41,6 +41,15 @@
  *   block; first use scanned row-major over (t, p); an out-of-range id sets an
  *   error bit and contributes nothing; a repeated id within a row sets an
  *   error bit and both uses are still computed.
+ *
+ * FP8 intermediate blocks (the opt-in low-precision variant):
+ *   MarloweAI/sgl-amd-mono-upstream PR #27 "each expert once", section
+ *   "Modifications": the AMD path keeps the SwiGLU intermediate in FP8 "mid
+ *   blocks" before down. The page gives no block size or scale; read here as
+ *   blocks of 32 consecutive intermediate values of one expert use, each block
+ *   with one power-of-two scale 2^k (the smallest with max|mid| <= 448 * 2^k,
+ *   k >= -126), each value replaced by its nearest OCP E4M3FN value at that
+ *   scale (ties to even).
  */
 #include <math.h>
 #include <stdint.h>
@@ -133,12 +142,55 @@ void oracle_w2_row(const oracle_weights *w, int H, int I, int e, int h, double *
 
 static double silu(double v) { return v / (1.0 + exp(-v)); }
 
+/* The nearest OCP E4M3FN value to v (ties to the even mantissa), saturating
+ * at +-448. E4M3FN: sign, 4 exponent bits (bias 7), 3 mantissa bits; normals
+ * 2^(e-7) (1 + m/8) for e = 1..15 (e = 15, m = 7 is NaN, so 448 is the
+ * largest); subnormals m 2^-9. On a grid of spacing `step` the nearest value
+ * with ties to even is nearbyint(a / step) * step (default rounding mode:
+ * to nearest, ties to even); the spacing is 2^-9 below 2^-6 and 2^(E-3) in the
+ * binade [2^E, 2^(E+1)). */
+double oracle_e4m3_rne(double v)
+{
+    double a = fabs(v), q;
+    if (a >= 448.0) {
+        q = 448.0;
+    } else if (a < ldexp(1.0, -6)) {
+        q = nearbyint(a / ldexp(1.0, -9)) * ldexp(1.0, -9);
+    } else {
+        int x;
+        (void)frexp(a, &x); /* a = f 2^x, f in [0.5, 1): binade exponent x - 1 */
+        double step = ldexp(1.0, x - 1 - 3);
+        q = nearbyint(a / step) * step;
+    }
+    return v < 0 ? -q : q;
+}
+
+/* In place: each block of `block` consecutive values shares the scale 2^k,
+ * the smallest power of two with max|mid| <= 448 * 2^k (k >= -126), and each
+ * value becomes its nearest E4M3 value at that scale. An all-zero block stays
+ * zero. 448 = 1.75 * 2^8, so with max|mid| = f 2^E (f in [1, 2)) the scale is
+ * k = E - 8, plus one when f > 1.75. */
+void oracle_fp8_mid_blocks(double *mid, int n, int block)
+{
+    for (int b0 = 0; b0 < n; b0 += block) {
+        int b1 = b0 + block < n ? b0 + block : n;
+        double amax = 0.0;
+        for (int i = b0; i < b1; ++i) amax = fabs(mid[i]) > amax ? fabs(mid[i]) : amax;
+        if (amax == 0.0) continue;
+        int x;
+        double f = frexp(amax, &x) * 2.0; /* amax = f 2^(x-1), f in [1, 2) */
+        int k = (x - 1) - 8 + (f > 1.75 ? 1 : 0);
+        if (k < -126) k = -126;
+        for (int i = b0; i < b1; ++i) mid[i] = ldexp(oracle_e4m3_rne(ldexp(mid[i], -k)), k);
+    }
+}
+
 /* One SwiGLU expert applied to one fp64 activation row:
  *   mid = silu(Wg x) .* (Wu x)     (Wg = rows 0..I-1, Wu = rows I..2I-1)
  *   y   = Wd mid
  * mid may be NULL. scratch needs max(H, I) doubles. */
-static void expert_ffn(const oracle_weights *w, int H, int I, int e,
-                       const double *x, double *mid, double *y, double *row)
+static void expert_ffn_q(const oracle_weights *w, int H, int I, int e,
+                         const double *x, double *mid, double *y, double *row, int fp8_block)
 {
     double *m = mid ? mid : (double *)malloc(sizeof(double) * (size_t)I);
     for (int i = 0; i < I; ++i) {
@@ -149,6 +201,7 @@ static void expert_ffn(const oracle_weights *w, int H, int I, int e,
         for (int h = 0; h < H; ++h) u += row[h] * x[h];
         m[i] = silu(g) * u;
     }
+    if (fp8_block > 0) oracle_fp8_mid_blocks(m, I, fp8_block);
     for (int h = 0; h < H; ++h) {
         double acc = 0.0;
         oracle_w2_row(w, H, I, e, h, row);
@@ -156,6 +209,12 @@ static void expert_ffn(const oracle_weights *w, int H, int I, int e,
         y[h] = acc;
     }
     if (!mid) free(m);
+}
+
+static void expert_ffn(const oracle_weights *w, int H, int I, int e,
+                       const double *x, double *mid, double *y, double *row)
+{
+    expert_ffn_q(w, H, I, e, x, mid, y, row, 0);
 }
 
 void oracle_expert_ffn(const oracle_weights *w, int H, int I, int e,
@@ -362,11 +421,38 @@ void oracle_moe_layer_rows(const uint16_t *x_bf16, const int32_t *ids,
  * threads, then each row summed in the same fixed order (x, shared, picks
  * 0..K-1) with the same operations, so the two agree bit for bit. Only the
  * scheduling differs: it lets one row's experts run in parallel. */
+static void layer_uses(const uint16_t *x_bf16, const int32_t *ids,
+                       const float *topk_w, const oracle_weights *routed,
+                       const oracle_weights *shared, int T, int H, int I,
+                       int I_shared, int E, int K, const int32_t *rows,
+                       int nrows, double *ref, int nthreads, int fp8_block);
+
 void oracle_moe_layer_uses(const uint16_t *x_bf16, const int32_t *ids,
                            const float *topk_w, const oracle_weights *routed,
                            const oracle_weights *shared, int T, int H, int I,
                            int I_shared, int E, int K, const int32_t *rows,
                            int nrows, double *ref, int nthreads)
+{
+    layer_uses(x_bf16, ids, topk_w, routed, shared, T, H, I, I_shared, E, K, rows, nrows, ref, nthreads, 0);
+}
+
+/* The layer with the FP8 intermediate blocks of the opt-in variant: every
+ * expert use's SwiGLU intermediate goes through oracle_fp8_mid_blocks with
+ * blocks of `block` values before down; the rest as oracle_moe_layer_uses. */
+void oracle_moe_layer_fp8mid(const uint16_t *x_bf16, const int32_t *ids,
+                             const float *topk_w, const oracle_weights *routed,
+                             const oracle_weights *shared, int T, int H, int I,
+                             int I_shared, int E, int K, const int32_t *rows,
+                             int nrows, double *ref, int nthreads, int block)
+{
+    layer_uses(x_bf16, ids, topk_w, routed, shared, T, H, I, I_shared, E, K, rows, nrows, ref, nthreads, block);
+}
+
+static void layer_uses(const uint16_t *x_bf16, const int32_t *ids,
+                       const float *topk_w, const oracle_weights *routed,
+                       const oracle_weights *shared, int T, int H, int I,
+                       int I_shared, int E, int K, const int32_t *rows,
+                       int nrows, double *ref, int nthreads, int fp8_block)
 {
     int K1 = K + 1, nuse = nrows * K1;
     double *Y = (double *)malloc(sizeof(double) * (size_t)(nuse > 0 ? nuse : 1) * (size_t)H);
@@ -385,10 +471,10 @@ void oracle_moe_layer_uses(const uint16_t *x_bf16, const int32_t *ids,
         double *y = Y + (size_t)u * H;
         for (int h = 0; h < H; ++h) x[h] = oracle_bf16(x_bf16[(size_t)t * H + h]);
         if (q == 0) {
-            expert_ffn(shared, H, I_shared, 0, x, NULL, y, row);
+            expert_ffn_q(shared, H, I_shared, 0, x, NULL, y, row, fp8_block);
         } else {
             int id = ids[t * K + q - 1];
-            if (id >= 0 && id < E) expert_ffn(routed, H, I, id, x, NULL, y, row);
+            if (id >= 0 && id < E) expert_ffn_q(routed, H, I, id, x, NULL, y, row, fp8_block);
         }
         free(x); free(row);
     }
