@@ -16,6 +16,7 @@ in four forms, alternating within every round: plain, chained (MOE_FLAG_CHAIN:
 each may start under the previous one), with the next layer's first
 shared-expert stages brought into L2 during each launch's tail
 (moe_fused_decode_next), and both. The T=8 and T=64 workloads are timed too, under `sweep`
+with the T=8 and T=64 layers again under the opt-in FP8 intermediate blocks
 (--no-sweep skips them); --sweep-wide adds the wide-expert layer (E=384 top-8, uniform routing) at
 T = 1, 2, 4, ..., 256 with 4 distinct layers' weights resident, run back to
 back, plain and chained. --impl reference times the fp64 CPU oracle on whole launches of the
@@ -46,6 +47,8 @@ WORKLOADS = {
 # (bf16 [E][H] gate, bf16 correction bias, top-8, renormalised, scale 2.5)
 # computed inside the same launch
 ROUTED = {"dsv3_t1_routed": dict(T=1)}
+# the opt-in FP8 intermediate blocks (MOE_FLAG_FP8_MID) on the workloads above
+FP8_MID = {"dsv3_t8_fp8mid": "dsv3_t8", "dsv3_t64_fp8mid": "dsv3_t64"}
 N_COPIES = 4
 HEAD_START_CYCLES = 4_000_000  # device sleep (about 2 ms) before a back-to-back timed region
 KERNEL_SOURCES = ["moe_layer_decode_persistent_b300/csrc/api.cu",
@@ -356,6 +359,9 @@ def run_ours(args, rank, world, local):
             sweep[name] = sweep_point(name, args, dev)
         for name in ROUTED:
             sweep[name] = routed_point(name, args, dev)
+        for name, base in FP8_MID.items():
+            sweep[name] = sweep_point(base, args, dev, B.MOE_FLAG_FP8_MID)
+            sweep[name]["flags"] = "MOE_FLAG_FP8_MID"
     wide = wide_sweep(args, dev) if args.sweep_wide else {}
     clk2.__exit__()
     return dict(us_launch=us_launch_max, ms_per_step=ms_per_step, algo_bytes=algo_bytes,
@@ -475,7 +481,7 @@ def back_to_back_us(launch, n: int) -> float:
     return a.elapsed_time(b) * 1e3 / n
 
 
-def sweep_point(name, args, dev):
+def sweep_point(name, args, dev, extra_flags: int = 0):
     """us per launch for another workload (same protocol, fewer steps)."""
     import torch
 
@@ -490,7 +496,7 @@ def sweep_point(name, args, dev):
                              for k, v in L.routed.__dict__.items()}), L.shared)
         for _ in range(N_COPIES - 1)]
     weights = [(B.make_weights(r), B.make_weights(s)) for r, s in copies]
-    sh = B.make_shape(shape.T, shape.H, shape.I, shape.I_shared, shape.E, shape.K, args.flags)
+    sh = B.make_shape(shape.T, shape.H, shape.I, shape.I_shared, shape.E, shape.K, args.flags | extra_flags)
     ws = torch.empty(B.moe_workspace_bytes(sh), dtype=torch.uint8, device=dev)
     B.moe_workspace_init(ws)
     out = torch.empty(shape.T, shape.H, dtype=torch.bfloat16, device=dev)

@@ -68,7 +68,7 @@ enum {
     MOE_FLAG_DEBUG_DROP_ARRIVE = 8u, /* fault injection: one CTA skips one
                                  inter-CTA arrival, so the waits on it time out
                                  and set MOE_DEV_WAIT_TIMEOUT */
-    MOE_FLAG_CHAIN = 16u      /* layers back to back: the launch may start
+    MOE_FLAG_CHAIN = 16u,     /* layers back to back: the launch may start
                                  while the previous kernel on the stream still
                                  runs (programmatic dependent launch). Each CTA
                                  sets up its barriers and tensor memory and
@@ -79,6 +79,19 @@ enum {
                                  and the previous kernel may produce this
                                  launch's inputs. Only weights must not be
                                  written by the previous kernel. */
+    MOE_FLAG_FP8_MID = 32u    /* opt-in low-precision variant (PR #27 "each
+                                 expert once", "Modifications": FP8 mid
+                                 blocks): the SwiGLU intermediate goes
+                                 through FP8 before down. Blocks of 32
+                                 consecutive intermediate values of one
+                                 column share the smallest power-of-two
+                                 scale 2^k with max|mid| <= 448 * 2^k
+                                 (k >= -126); each value becomes its nearest
+                                 OCP E4M3FN value (ties to even) times 2^k.
+                                 Tensor-core path only: with
+                                 MOE_FLAG_FORCE_FMA, or where the tensor-core
+                                 path is not eligible, the call fails with
+                                 MOE_ERR_UNSUPPORTED. */
 };
 
 /* Weight storage formats. */

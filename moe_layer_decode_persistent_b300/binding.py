@@ -16,6 +16,7 @@ LIB_PATH = os.path.join(PKG, "libmoe.so")
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA = range(5)
 MOE_DEV_BAD_EXPERT, MOE_DEV_DUP_EXPERT, MOE_DEV_WAIT_TIMEOUT, MOE_DEV_RANGE = 1, 2, 4, 8
 MOE_FLAG_NO_DEDUP, MOE_FLAG_FORCE_FMA, MOE_FLAG_FORCE_MMA, MOE_FLAG_DEBUG_DROP_ARRIVE, MOE_FLAG_CHAIN = 1, 2, 4, 8, 16
+MOE_FLAG_FP8_MID = 32
 MOE_W_BF16, MOE_W_NVFP4, MOE_W_FP8_B128 = 0, 1, 2
 
 # every symbol include/moe.h declares

@@ -146,7 +146,7 @@ moe_status check_shape(const moe_shape *s) {
             return fail(MOE_ERR_UNSUPPORTED, "%s=%d is not a multiple of 128", names[i], dims[i]);
     }
     const unsigned known = MOE_FLAG_NO_DEDUP | MOE_FLAG_FORCE_FMA | MOE_FLAG_FORCE_MMA |
-                           MOE_FLAG_DEBUG_DROP_ARRIVE | MOE_FLAG_CHAIN;
+                           MOE_FLAG_DEBUG_DROP_ARRIVE | MOE_FLAG_CHAIN | MOE_FLAG_FP8_MID;
     if (s->flags & ~known) return fail(MOE_ERR_INVALID_ARG, "unknown flag bits 0x%x", s->flags & ~known);
     if ((s->flags & MOE_FLAG_FORCE_FMA) && (s->flags & MOE_FLAG_FORCE_MMA))
         return fail(MOE_ERR_INVALID_ARG, "FORCE_FMA and FORCE_MMA both set");
@@ -226,7 +226,7 @@ moe_status dev_info(int dev, DevInfo *out) {
         e = cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
         if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(smem)");
         cudaFuncAttributes fa;
-        e = cudaFuncGetAttributes(&fa, moe::fused_tc_kernel<false, false>);
+        e = cudaFuncGetAttributes(&fa, moe::fused_tc_kernel<false, false, false>);
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncGetAttributes");
         d.tc_static_smem = (int)fa.sharedSizeBytes;
         g_dev[dev] = d;
@@ -533,8 +533,11 @@ moe_status launch_fused_tc(const moe::FusedParams &fp, const WsLayout &L, const 
     int occ = 0;
     const bool capped = moe::tc_capped_tables(s->T);
     void (*kern)(const moe::TcParams) =
-        p.route_mode ? (capped ? moe::fused_tc_kernel<true, true> : moe::fused_tc_kernel<false, true>)
-                     : (capped ? moe::fused_tc_kernel<true, false> : moe::fused_tc_kernel<false, false>);
+        !(s->flags & MOE_FLAG_FP8_MID)
+            ? (p.route_mode ? (capped ? moe::fused_tc_kernel<true, true, false> : moe::fused_tc_kernel<false, true, false>)
+                            : (capped ? moe::fused_tc_kernel<true, false, false> : moe::fused_tc_kernel<false, false, false>))
+            : (p.route_mode ? (capped ? moe::fused_tc_kernel<true, true, true> : moe::fused_tc_kernel<false, true, true>)
+                            : (capped ? moe::fused_tc_kernel<true, false, true> : moe::fused_tc_kernel<false, false, true>));
     if ((st = plan_occupancy(kern, dev, moe::kTcThreads, smem, d, &occ)) != MOE_OK) return st;
     cudaLaunchConfig_t cfg = {};
     if (d.nsm > moe::kTcMaxGrid)
@@ -633,6 +636,9 @@ moe_status fused_decode_impl(const void *x, const int32_t *ids, const float *w,
     bool use_tc = tc_ok && !(s->flags & MOE_FLAG_FORCE_FMA);
     if ((s->flags & MOE_FLAG_FORCE_MMA) && !tc_ok)
         return fail(MOE_ERR_UNSUPPORTED, "tensor-core path requested but unavailable: %s", why);
+    if ((s->flags & MOE_FLAG_FP8_MID) && !use_tc)
+        return fail(MOE_ERR_UNSUPPORTED, "MOE_FLAG_FP8_MID needs the tensor-core path: %s",
+                    tc_ok ? "MOE_FLAG_FORCE_FMA is set" : why);
     const size_t need = router ? L.dev_total : use_tc ? L.tc_end : fma_need;
     if (ws_bytes < need)
         return fail(MOE_ERR_WORKSPACE, "workspace has %zu B, needs %zu B", ws_bytes, need);

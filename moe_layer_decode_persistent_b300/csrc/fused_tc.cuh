@@ -59,6 +59,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_fp8.h>
 
 #include "group_table.cuh"
 #include "moe_common.cuh"
@@ -362,10 +363,31 @@ __device__ __forceinline__ float swiglu_scaled(float g, float u, float fs, float
 }
 __device__ __forceinline__ float pow2f(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }  // |e| <= 126
 
+// FP8 intermediate blocks (MOE_FLAG_FP8_MID; PR #27 "each expert once",
+// "Modifications": FP8 mid blocks). The warp's 32 values of one column (one
+// per lane: 32 consecutive intermediate rows) share the smallest power-of-two
+// scale 2^k with max|m| <= 448 * 2^k (k >= -126), and each becomes its nearest
+// E4M3 value (ties to even) times 2^k, which f16 then holds exactly. 448 is
+// 1.75 * 2^8, so with max|m| = f 2^E (f in [1, 2)) k = E - 8, plus one when
+// f > 1.75. Warp-collective; an all-zero or non-finite block is left as it is
+// (the range check flags the latter).
+__device__ __forceinline__ float fp8_mid_q(float m) {
+    float a = fabsf(m);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    const uint32_t b = __float_as_uint(a);
+    if (a == 0.0f || b >= 0x7f800000u) return m;
+    const int k = max((int)(b >> 23) - 127 - 8 + ((b & 0x7fffffu) > 0x600000u ? 1 : 0), -126);
+    const __nv_fp8_storage_t q = __nv_cvt_float_to_fp8(__fmul_rn(m, pow2f(-k)), __NV_SATFINITE, __NV_E4M3);
+    return __fmul_rn(__half2float(__half(__nv_cvt_fp8_to_halfraw(q, __NV_E4M3))), pow2f(k));
+}
+
 // kRouted: the picks and weights come from the router inside the launch (a
 // separate instantiation, so the router's registers never weigh on the
 // unrouted kernel's hot loops).
-template <bool kCappedTables, bool kRouted>
+// kFp8Mid: the opt-in FP8 intermediate blocks, an instantiation of its own so
+// the default kernels' code is unchanged by it.
+template <bool kCappedTables, bool kRouted, bool kFp8Mid>
 __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_constant__ TcParams p) {
     using namespace sm100;
     extern __shared__ __align__(1024) uint8_t smem_raw_[];
@@ -1137,6 +1159,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
         // skips its first intermediate-ready arrival, so the down jobs of that
         // (group, column tile) wait out their budget and the launch aborts
         bool drop_next = (p.flags & kFlagDebugDropArrive) && blockIdx.x == 0 && quarter == 0;
+        constexpr bool fp8mid = kFp8Mid;
         for (;;) {
             if (!__all_sync(0xffffffffu, mbar_wait(&jfull[js], jph, abort_flag, err))) break;
             const TcJob d = job_at(js);
@@ -1181,7 +1204,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                         } else {
                             const int sx = xsc ? xs_s[crow[col]] : 0;
                             const float m = swiglu_scaled(__fmul_rn(v0, gs13), __fmul_rn(v1, gs13), pow2f(sx), pow2f(-sx));
-                            const __half hm = __float2half_rn(m);
+                            const __half hm = __float2half_rn(fp8mid ? fp8_mid_q(m) : m);
                             if (__hisinf(hm) || !(fabsf(m) == fabsf(m))) range_bad = 1;
                             *reinterpret_cast<__half *>(mb + b_off(c, r)) = hm;
                         }
@@ -1296,7 +1319,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fused_tc_kernel(const __grid_co
                             }
                             const int sx = xsc ? xs_s[crow[col]] : 0;
                             const float m = swiglu_scaled(__fmul_rn(sg, gs13), __fmul_rn(su, gs13), pow2f(sx), pow2f(-sx));
-                            const __half hm = __float2half_rn(m);
+                            const __half hm = __float2half_rn(fp8mid ? fp8_mid_q(m) : m);
                             if (__hisinf(hm) || !(fabsf(m) == fabsf(m))) range_bad = 1;
                             *reinterpret_cast<__half *>(mb + b_off(c, r)) = hm;
                         }

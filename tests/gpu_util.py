@@ -63,7 +63,7 @@ def oracle_weightset(es):
                             es.w2_gscale)
 
 
-def oracle_ref(L, rows=None, threads=None):
+def oracle_ref(L, rows=None, threads=None, fp8_mid=False):
     """fp64 reference rows, copying to the host only the routed experts used."""
     s = L.shape
     ids = L.topk_ids.cpu().numpy().astype(np.int64)
@@ -74,8 +74,9 @@ def oracle_ref(L, rows=None, threads=None):
     routed = oracle_weightset(L.routed.select(used)) if used else oracle_weightset(L.routed.select([0]))
     shared = oracle_weightset(L.shared.to("cpu"))
     threads = threads or min(32, os.cpu_count() or 1)
-    return oracle.moe_layer(L.x.cpu(), ids2, L.topk_w.cpu(), routed, shared, s.T, s.H, s.I,
-                            s.I_shared, max(len(used), 1), s.K, rows=rows, threads=threads)
+    f = oracle.moe_layer_fp8mid if fp8_mid else oracle.moe_layer
+    return f(L.x.cpu(), ids2, L.topk_w.cpu(), routed, shared, s.T, s.H, s.I, s.I_shared, max(len(used), 1), s.K,
+             rows=rows, threads=threads)
 
 
 # (test id, worst |err|/bound, elements compared) of every parity check in

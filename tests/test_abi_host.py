@@ -54,7 +54,7 @@ def test_workspace_bytes_grow_with_T_and_reject_bad_shapes():
 def test_every_declared_flag_is_accepted_and_leaves_the_workspace_size():
     base = B.moe_workspace_bytes(_shape(T=8))
     for f in (B.MOE_FLAG_NO_DEDUP, B.MOE_FLAG_FORCE_FMA, B.MOE_FLAG_FORCE_MMA, B.MOE_FLAG_DEBUG_DROP_ARRIVE,
-              B.MOE_FLAG_CHAIN, B.MOE_FLAG_CHAIN | B.MOE_FLAG_FORCE_MMA):
+              B.MOE_FLAG_CHAIN, B.MOE_FLAG_CHAIN | B.MOE_FLAG_FORCE_MMA, B.MOE_FLAG_FP8_MID):
         assert B.moe_workspace_bytes(_shape(T=8, flags=f)) == base, f
 
 
